@@ -1,0 +1,294 @@
+"""Pins of the FP64 CPU oracle to facts the pages and the mathematics fix.
+
+None of these re-types the oracle's own formula: each checks a property that
+a correct attention must have and that a plausible slip in the oracle (a
+dropped term, a wrong sign or index, a transposed operand, a wrong mask or
+scale) would break.  All run on the CPU in well under a minute.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import fa_inputs
+
+
+def _scale(d):
+    # the API takes scale as a C float; the oracle promotes that float to double
+    return float(np.float32(1.0 / math.sqrt(d)))
+
+
+def _rand(seed, B, H, N, d):
+    x = fa_inputs.attention_inputs(seed, B, H, N, d, "f32")
+    return x["q"], x["k"], x["v"], x["do"]
+
+
+# ---------------------------------------------------------------- softmax rows
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probability_rows_sum_to_one(oracle_lib, causal):
+    q, k, _, _ = _rand(11, 1, 1, 37, 8)
+    p = oracle_lib.attention_probs(q[0, 0], k[0, 0], causal, _scale(8))
+    assert np.all(p >= 0.0)
+    assert np.max(np.abs(p.sum(axis=1) - 1.0)) <= 1e-12
+    if causal:  # key j visible to query i iff j <= i
+        assert np.all(np.triu(p, 1) == 0.0)
+        assert np.all(np.diag(p) > 0.0)
+    else:
+        assert np.all(p > 0.0)
+
+
+# ------------------------------------------------- online-softmax merge (page 3)
+
+def _block_stats(oracle_lib, q, k, v, scale):
+    """Normalised O, block max m and l = sum exp(s - m) of one key block."""
+    o, lse = oracle_lib.attention_fwd(q, k, v, False, scale)
+    s = scale * np.einsum("bhid,bhjd->bhij", q.astype(np.float64), k.astype(np.float64))
+    m = s.max(axis=-1)
+    l = np.exp(lse - m)
+    return o, m, l
+
+
+def _merge(o1, m1, l1, o2_unnorm, m2, l2):
+    """The two-block merge of the online-softmax page (section 2): O1 is the
+    normalised running output, O2 the unnormalised block product."""
+    m = np.maximum(m1, m2)
+    l = l1 * np.exp(m1 - m) + l2 * np.exp(m2 - m)
+    o = (o1 * (l1 * np.exp(m1 - m) / l)[..., None]
+         + o2_unnorm * (np.exp(m2 - m) / l)[..., None])
+    return o, m, l
+
+
+def test_two_block_merge_equals_full_softmax_at_every_cut(oracle_lib):
+    B, H, N, d = 1, 2, 12, 6
+    q, k, v, _ = _rand(12, B, H, N, d)
+    s = _scale(d)
+    o_full, lse_full = oracle_lib.attention_fwd(q, k, v, False, s)
+    for cut in range(1, N):
+        o1, m1, l1 = _block_stats(oracle_lib, q, k[:, :, :cut], v[:, :, :cut], s)
+        o2, m2, l2 = _block_stats(oracle_lib, q, k[:, :, cut:], v[:, :, cut:], s)
+        o, m, l = _merge(o1, m1, l1, o2 * l2[..., None], m2, l2)
+        assert np.max(np.abs(o - o_full)) <= 1e-12, cut
+        assert np.max(np.abs(m + np.log(l) - lse_full)) <= 1e-12, cut
+
+
+def test_three_way_fold_equals_full_softmax(oracle_lib):
+    B, H, N, d = 2, 1, 15, 4
+    q, k, v, _ = _rand(13, B, H, N, d)
+    s = _scale(d)
+    o_full, lse_full = oracle_lib.attention_fwd(q, k, v, False, s)
+    cuts = [(0, 4), (4, 11), (11, 15)]
+    o, m, l = _block_stats(oracle_lib, q, k[:, :, 0:4], v[:, :, 0:4], s)
+    for a, b in cuts[1:]:
+        o2, m2, l2 = _block_stats(oracle_lib, q, k[:, :, a:b], v[:, :, a:b], s)
+        o, m, l = _merge(o, m, l, o2 * l2[..., None], m2, l2)
+    assert np.max(np.abs(o - o_full)) <= 1e-12
+    assert np.max(np.abs(m + np.log(l) - lse_full)) <= 1e-12
+
+
+def _buggy_blocked_snippet(q, k, v, block, scale):
+    """Restatement of the blocked PyTorch example on the Hindi page
+    ("implementation details"): it keeps O already divided by L, yet rescales
+    it by exp(M - M_new) alone before dividing by L_new, dropping the old L."""
+    q, k, v = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
+    n = q.shape[0]
+    o = np.zeros_like(q)
+    lsum = np.zeros(n)
+    mx = np.full(n, -np.inf)
+    for i in range(0, n, block):
+        rows = slice(i, i + block)
+        for j in range(0, n, block):
+            sblk = scale * q[rows] @ k[j:j + block].T
+            m_new = np.maximum(mx[rows], sblk.max(axis=1))
+            e = np.exp(sblk - m_new[:, None])
+            a = np.exp(mx[rows] - m_new)
+            l_new = a * lsum[rows] + e.sum(axis=1)
+            o[rows] = (a[:, None] * o[rows] + e @ v[j:j + block]) / l_new[:, None]
+            lsum[rows] = l_new
+            mx[rows] = m_new
+    return o
+
+
+def test_oracle_differs_from_the_buggy_blocked_example(oracle_lib):
+    N, d, block = 40, 8, 16
+    q, k, v, _ = _rand(14, 1, 1, N, d)
+    s = _scale(d)
+    o, _ = oracle_lib.attention_fwd(q, k, v, False, s)
+    # one block: the missing factor is L_old = 0, so the example is right
+    one = _buggy_blocked_snippet(q[0, 0], k[0, 0], v[0, 0], N, s)
+    assert np.max(np.abs(one - o[0, 0])) <= 1e-12
+    # several blocks: the example is wrong and the oracle must not follow it
+    many = _buggy_blocked_snippet(q[0, 0], k[0, 0], v[0, 0], block, s)
+    assert np.max(np.abs(many - o[0, 0])) > 1e-2
+
+
+# ------------------------------------------------------------- closed forms
+
+def test_single_key_returns_v_and_its_score(oracle_lib):
+    q, k, v, _ = _rand(15, 2, 3, 1, 16)
+    s = _scale(16)
+    for causal in (False, True):
+        o, lse = oracle_lib.attention_fwd(q, k, v, causal, s)
+        assert np.array_equal(o, v.astype(np.float64))
+        for b in range(2):
+            for h in range(3):
+                want = s * math.fsum(float(x) * float(y) for x, y in zip(q[b, h, 0], k[b, h, 0]))
+                assert abs(lse[b, h, 0] - want) <= 1e-12
+
+
+def test_constant_value_rows(oracle_lib):
+    B, H, N, d = 1, 2, 9, 5
+    q, k, _, _ = _rand(16, B, H, N, d)
+    row = np.array([0.5, -1.25, 3.0, 0.0, 2.0])
+    v = np.broadcast_to(row, (B, H, N, d)).copy()
+    for causal in (False, True):
+        o, _ = oracle_lib.attention_fwd(q, k, v, causal, _scale(d))
+        assert np.max(np.abs(o - row)) <= 1e-14
+
+
+def test_first_causal_query(oracle_lib):
+    B, H, N, d = 2, 2, 7, 8
+    q, k, v, _ = _rand(17, B, H, N, d)
+    s = _scale(d)
+    o, lse = oracle_lib.attention_fwd(q, k, v, True, s)
+    assert np.array_equal(o[:, :, 0], v[:, :, 0].astype(np.float64))
+    want = s * np.einsum("bhd,bhd->bh", q[:, :, 0].astype(np.float64), k[:, :, 0].astype(np.float64))
+    assert np.max(np.abs(lse[:, :, 0] - want)) <= 1e-12
+
+
+def test_uniform_scores_forward(oracle_lib):
+    B, H, N, d = 1, 1, 10, 4
+    q, _, v, _ = _rand(18, B, H, N, d)
+    k = np.zeros_like(q)
+    o, lse = oracle_lib.attention_fwd(q, k, v, False, 0.3)
+    assert np.max(np.abs(o - v.astype(np.float64).mean(axis=2, keepdims=True))) <= 1e-14
+    assert np.max(np.abs(lse - math.log(N))) <= 1e-14
+    o, lse = oracle_lib.attention_fwd(q, k, v, True, 0.3)
+    prefix = np.cumsum(v.astype(np.float64), axis=2) / np.arange(1, N + 1)[:, None]
+    assert np.max(np.abs(o - prefix)) <= 1e-14
+    assert np.max(np.abs(lse[0, 0] - np.log(np.arange(1, N + 1)))) <= 1e-14
+
+
+def test_uniform_scores_causal_dv(oracle_lib):
+    B, H, N, d = 1, 1, 8, 3
+    q, _, v, do = _rand(19, B, H, N, d)
+    k = np.zeros_like(q)
+    _, _, dv, _ = oracle_lib.attention_bwd(q, k, v, do, True, 0.7)
+    do64 = do[0, 0].astype(np.float64)
+    for j in range(N):
+        want = sum(do64[i] / (i + 1) for i in range(j, N))
+        assert np.max(np.abs(dv[0, j] - want)) <= 1e-14
+
+
+# ------------------------------------------------------------- invariances
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_shift_invariance(oracle_lib, causal):
+    B, H, N, d = 1, 2, 11, 4
+    q, k, v, _ = _rand(20, B, H, N, d)
+    u = np.array([0.25, -0.5, 1.0, 0.125])
+    s = _scale(d)
+    o, lse = oracle_lib.attention_fwd(q, k, v, causal, s)
+    o2, lse2 = oracle_lib.attention_fwd(q, k + u, v, causal, s)
+    assert np.max(np.abs(o2 - o)) <= 1e-12
+    assert np.max(np.abs(lse2 - (lse + s * q.astype(np.float64) @ u))) <= 1e-12
+
+
+def test_permutation_invariance(oracle_lib):
+    B, H, N, d = 1, 1, 13, 6
+    q, k, v, _ = _rand(21, B, H, N, d)
+    s = _scale(d)
+    o, lse = oracle_lib.attention_fwd(q, k, v, False, s)
+    perm = np.random.default_rng(0).permutation(N)
+    o_kv, lse_kv = oracle_lib.attention_fwd(q, k[:, :, perm], v[:, :, perm], False, s)
+    assert np.max(np.abs(o_kv - o)) <= 1e-12
+    assert np.max(np.abs(lse_kv - lse)) <= 1e-12
+    o_q, lse_q = oracle_lib.attention_fwd(q[:, :, perm], k, v, False, s)
+    assert np.max(np.abs(o_q - o[:, :, perm])) <= 1e-14
+    assert np.max(np.abs(lse_q - lse[:, :, perm])) <= 1e-14
+
+
+def test_rows_entry_matches_full_forward(oracle_lib):
+    B, H, N, d = 2, 3, 20, 8
+    q, k, v, _ = _rand(22, B, H, N, d)
+    s = _scale(d)
+    for causal in (False, True):
+        o, lse = oracle_lib.attention_fwd(q, k, v, causal, s)
+        heads = np.array([0, 5, 3, 1, 2])
+        rows = np.array([0, 19, 7, 1, 13])
+        orow, lrow = oracle_lib.attention_fwd_rows(q, k, v, causal, s, heads, rows)
+        assert np.array_equal(orow, o.reshape(B * H, N, d)[heads, rows])
+        assert np.array_equal(lrow, lse.reshape(B * H, N)[heads, rows])
+
+
+# ------------------------------------------------------------- gradients
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradient_identities(oracle_lib, causal):
+    B, H, N, d = 2, 1, 9, 5
+    q, k, v, do = _rand(23, B, H, N, d)
+    s = _scale(d)
+    dq, dk, dv, dvec = oracle_lib.attention_bwd(q, k, v, do, causal, s)
+    dk = dk.reshape(B, H, N, d)
+    dv = dv.reshape(B, H, N, d)
+    # rows of dS sum to zero, so the keys' gradients sum to zero
+    assert np.max(np.abs(dk.sum(axis=2))) <= 1e-12
+    # each query's probabilities sum to one, so sum_j dV_j = sum_i dO_i
+    assert np.max(np.abs(dv.sum(axis=2) - do.astype(np.float64).sum(axis=2))) <= 1e-12
+    # D_i = dO_i . O_i = sum_j P_ij dP_ij
+    for b in range(B):
+        p = oracle_lib.attention_probs(q[b, 0], k[b, 0], causal, s)
+        dp = do[b, 0].astype(np.float64) @ v[b, 0].astype(np.float64).T
+        assert np.max(np.abs((p * dp).sum(axis=1) - dvec[b])) <= 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d", [(1, 2), (5, 3), (8, 4)])
+def test_backward_matches_finite_differences(oracle_lib, causal, N, d):
+    q, k, v, do = (t.astype(np.float64) for t in _rand(24 + N, 1, 1, N, d))
+    s = 0.6
+
+    def loss(qq, kk, vv):
+        o, _ = oracle_lib.attention_fwd(qq, kk, vv, causal, s)
+        return float((do * o).sum())
+
+    dq, dk, dv, _ = oracle_lib.attention_bwd(q, k, v, do, causal, s)
+    h = 1e-6
+    for grad, which in ((dq, 0), (dk, 1), (dv, 2)):
+        num = np.zeros((N, d))
+        for i in range(N):
+            for c in range(d):
+                args_p = [q.copy(), k.copy(), v.copy()]
+                args_m = [q.copy(), k.copy(), v.copy()]
+                args_p[which][0, 0, i, c] += h
+                args_m[which][0, 0, i, c] -= h
+                num[i, c] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        scale_ref = max(1.0, np.max(np.abs(num)))
+        assert np.max(np.abs(grad[0] - num)) <= 1e-6 * scale_ref, which
+
+
+def test_backward_head_selection(oracle_lib):
+    B, H, N, d = 2, 2, 6, 4
+    q, k, v, do = _rand(30, B, H, N, d)
+    full = oracle_lib.attention_bwd(q, k, v, do, True, 0.5)
+    heads = np.array([3, 0])
+    part = oracle_lib.attention_bwd(q, k, v, do, True, 0.5, heads=heads)
+    for a, b in zip(full, part):
+        assert np.array_equal(a[heads], b)
+
+
+def test_backward_d_uses_exact_forward_output(oracle_lib):
+    B, H, N, d = 1, 1, 7, 3
+    q, k, v, do = _rand(31, B, H, N, d)
+    o, _ = oracle_lib.attention_fwd(q, k, v, True, 0.5)
+    _, _, _, dvec = oracle_lib.attention_bwd(q, k, v, do, True, 0.5)
+    assert np.max(np.abs(dvec[0] - (do[0, 0].astype(np.float64) * o[0, 0]).sum(axis=1))) <= 1e-14
+
+
+def test_oracle_rejects_bad_arguments(oracle_lib):
+    q = np.zeros((1, 1, 4, 2))
+    with pytest.raises(RuntimeError):
+        oracle_lib.attention_fwd_rows(q, q, q, False, 1.0, np.array([1]), np.array([0]))
+    with pytest.raises(RuntimeError):
+        oracle_lib.attention_fwd_rows(q, q, q, False, 1.0, np.array([0]), np.array([4]))

@@ -53,7 +53,9 @@ def _load():
                                         ctypes.c_double, _ip, _ip, _i64, _dp, _dp]
         lib.oracle_probs.argtypes = [_dp, _dp, _i64, _i64, ctypes.c_int, ctypes.c_double, _dp]
         lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64, ctypes.c_int,
-                                   ctypes.c_double, _ip, _i64, _dp, _dp, _dp, _dp]
+                                   ctypes.c_double, ctypes.c_int, _ip, _i64, _dp, _dp, _dp, _dp]
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_round_bf16.restype = ctypes.c_double
         for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_probs, lib.oracle_bwd,
                   lib.oracle_num_threads):
             f.restype = ctypes.c_int
@@ -126,8 +128,24 @@ def attention_probs(q, k, causal: bool, scale: float) -> np.ndarray:
     return p
 
 
-def attention_bwd(q, k, v, do, causal: bool, scale: float, heads=None):
-    """dQ, dK, dV [n, N, d] and D [n, N] for the listed heads (all when None)."""
+_O_STORAGE = {"exact": 0, "bf16": 1, "f32": 2}
+
+
+def round_bf16(x: float) -> float:
+    """x rounded to the nearest bfloat16 value, ties to even (normal range)."""
+    return float(_load().oracle_round_bf16(float(x)))
+
+
+def attention_bwd(q, k, v, do, causal: bool, scale: float, heads=None, o_storage="exact"):
+    """dQ, dK, dV [n, N, d] and D [n, N] for the listed heads (all when None).
+
+    o_storage names the precision the output O is stored in before the
+    backward forms D = rowsum(dO o O): "exact" (FP64, the true gradient of the
+    exact function), "bf16" or "f32" (O rounded to the storage type the
+    backward is handed).
+    """
+    if o_storage not in _O_STORAGE:
+        raise ValueError(f"o_storage must be one of {sorted(_O_STORAGE)}")
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, d = q.shape
     if heads is None:
@@ -142,6 +160,7 @@ def attention_bwd(q, k, v, do, causal: bool, scale: float, heads=None):
     dv = np.empty_like(dq)
     dvec = np.empty((n, N), dtype=np.float64)
     _check(_load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, N, d, int(causal),
-                              float(scale), hp, n, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dvec)),
+                              float(scale), _O_STORAGE[o_storage], hp, n, _ptr(dq), _ptr(dk),
+                              _ptr(dv), _ptr(dvec)),
            "oracle_bwd")
     return dq, dk, dv, dvec

@@ -30,6 +30,13 @@
  * instead of storing it (page 4, "recomputation"); these formulas are the
  * plainest reading and are pinned by finite differences in the tests.
  *
+ * D is the row sum of dO o O over the output O the backward is handed.  The
+ * method stores O in the output precision (bf16 for bf16 inputs, fp32 for
+ * fp32 inputs) and its backward forms D from that stored tensor, so the
+ * backward takes o_storage: 0 uses the exact FP64 O (the true gradient of the
+ * exact function), 1 rounds the FP64 O to bf16 (nearest, ties to even) and 2
+ * rounds it to fp32 before D is formed.  Nothing else changes.
+ *
  * All inputs are float64 arrays in [B, H, N, d] row-major layout (the caller
  * converts bf16 / fp32 inputs exactly).  Work is spread over (b, h) heads or
  * sampled rows with OpenMP; every head or row is computed on its own, so the
@@ -170,11 +177,27 @@ int oracle_probs(const double* q, const double* k, int64_t N, int64_t d, int cau
     return 0;
 }
 
+/* x rounded to the nearest bfloat16 value (8 significant bits), ties to even.
+ * Written for the normal range; zero, infinities and NaN pass through. */
+double oracle_round_bf16(double x) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    double m = frexp(x, &e);          /* x = m 2^e, 0.5 <= |m| < 1 */
+    double r = nearbyint(ldexp(m, 8)); /* default rounding mode: nearest, ties to even */
+    return ldexp(r, e - 8);
+}
+
+static double stored_output(double x, int o_storage) {
+    if (o_storage == 1) return oracle_round_bf16(x);
+    if (o_storage == 2) return (double)(float)x;
+    return x;
+}
+
 /* Backward of one head with explicit N x N matrices.  All pointers are the
  * head's own [N, d] (or [N]) slices.  Scratch: 2 N^2 + N d doubles. */
 static int backward_head(const double* qh, const double* kh, const double* vh,
                          const double* doh, int64_t N, int64_t d, int causal, double scale,
-                         double* dqh, double* dkh, double* dvh, double* dh) {
+                         int o_storage, double* dqh, double* dkh, double* dvh, double* dh) {
     double* P = (double*)malloc(sizeof(double) * (size_t)(N * N));
     double* dS = (double*)malloc(sizeof(double) * (size_t)(N * N));
     double* O = (double*)malloc(sizeof(double) * (size_t)(N * d));
@@ -199,7 +222,7 @@ static int backward_head(const double* qh, const double* kh, const double* vh,
     /* D_i = dO_i . O_i, then dS = P o (dP - D), dP_ij = dO_i . V_j */
     for (int64_t i = 0; i < N; ++i) {
         double Di = 0.0;
-        for (int64_t c = 0; c < d; ++c) Di += doh[i * d + c] * O[i * d + c];
+        for (int64_t c = 0; c < d; ++c) Di += doh[i * d + c] * stored_output(O[i * d + c], o_storage);
         if (dh) dh[i] = Di;
         for (int64_t j = 0; j < N; ++j) {
             double dP = 0.0;
@@ -229,12 +252,14 @@ static int backward_head(const double* qh, const double* kh, const double* vh,
 
 /* Backward on a list of whole heads.  heads[s] (b * H + h) selects the s-th
  * head computed; heads == NULL means all B*H heads in order.  Outputs are
- * packed per computed head: dq/dk/dv [n, N, d], dvec [n, N] (D, may be NULL). */
+ * packed per computed head: dq/dk/dv [n, N, d], dvec [n, N] (D, may be NULL).
+ * o_storage selects the O that D is formed from (0 exact, 1 bf16, 2 fp32). */
 int oracle_bwd(const double* q, const double* k, const double* v, const double* dO,
                int64_t B, int64_t H, int64_t N, int64_t d, int causal, double scale,
-               const int64_t* heads, int64_t n, double* dq, double* dk, double* dv,
-               double* dvec) {
+               int o_storage, const int64_t* heads, int64_t n, double* dq, double* dk,
+               double* dv, double* dvec) {
     if (!q || !k || !v || !dO || !dq || !dk || !dv || bad_shape(B, H, N, d)) return -1;
+    if (o_storage < 0 || o_storage > 2) return -1;
     if (!heads) n = B * H;
     if (n < 0) return -1;
     if (heads)
@@ -246,7 +271,7 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
         int64_t bh = heads ? heads[s] : s;
         int64_t off = bh * N * d;
         int rc = backward_head(q + off, k + off, v + off, dO + off, N, d, causal, scale,
-                               dq + s * N * d, dk + s * N * d, dv + s * N * d,
+                               o_storage, dq + s * N * d, dk + s * N * d, dv + s * N * d,
                                dvec ? dvec + s * N : NULL);
         if (rc) {
 #pragma omp atomic write

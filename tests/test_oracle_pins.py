@@ -292,3 +292,51 @@ def test_oracle_rejects_bad_arguments(oracle_lib):
         oracle_lib.attention_fwd_rows(q, q, q, False, 1.0, np.array([1]), np.array([0]))
     with pytest.raises(RuntimeError):
         oracle_lib.attention_fwd_rows(q, q, q, False, 1.0, np.array([0]), np.array([4]))
+
+
+# ------------------------------------------------- D from the stored output
+
+def test_round_bf16_fixed_values(oracle_lib):
+    r = oracle_lib.round_bf16
+    for exact in (1.0, -2.5, 0.15625, 3.140625, 2.0 ** -100, -(2.0 ** 100), 0.0):
+        assert r(exact) == exact
+    assert r(1.0 + 2.0 ** -8) == 1.0                       # tie, even neighbour below
+    assert r(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6       # tie, even neighbour above
+    assert r(1.0 + 0.7 * 2.0 ** -7) == 1.0 + 2.0 ** -7     # nearest
+    assert r(300.5) == 300.0                               # spacing 2 between 256 and 512
+    assert r(-(1.0 + 3 * 2.0 ** -8)) == -(1.0 + 2.0 ** -6)
+
+
+def test_round_bf16_matches_float32_bit_rounding(oracle_lib):
+    # float32 inputs: a single rounding either way, so the two independent
+    # implementations (frexp/nearbyint in the oracle, integer bit arithmetic in
+    # the input generator) must agree exactly.
+    x = np.random.default_rng(5).standard_normal(20000).astype(np.float32) * 7
+    want = fa_inputs.bf16_to_f32(fa_inputs.bf16_bits(x)).astype(np.float64)
+    got = np.array([oracle_lib.round_bf16(float(t)) for t in x])
+    assert np.array_equal(got, want)
+
+
+def test_stored_output_d(oracle_lib):
+    B, H, N, d = 1, 1, 7, 6
+    q, k, v, do = _rand(32, B, H, N, d)
+    o, _ = oracle_lib.attention_fwd(q, k, v, True, 0.5)
+    *_, d_exact = oracle_lib.attention_bwd(q, k, v, do, True, 0.5)
+    *_, d_bf16 = oracle_lib.attention_bwd(q, k, v, do, True, 0.5, o_storage="bf16")
+    *_, d_f32 = oracle_lib.attention_bwd(q, k, v, do, True, 0.5, o_storage="f32")
+    do64 = do[0, 0].astype(np.float64)
+    o_b = fa_inputs.bf16_to_f32(fa_inputs.bf16_bits(o[0, 0].astype(np.float32))).astype(np.float64)
+    assert np.max(np.abs(d_bf16[0] - (do64 * o_b).sum(axis=1))) <= 1e-12
+    o_f = o[0, 0].astype(np.float32).astype(np.float64)
+    assert np.max(np.abs(d_f32[0] - (do64 * o_f).sum(axis=1))) <= 1e-12
+    assert np.max(np.abs(d_bf16 - d_exact)) > 1e-6  # the rounding is really applied
+
+
+def test_stored_output_is_exact_when_o_is_representable(oracle_lib):
+    # One key: O = V, which is already a bf16 value, so rounding O changes nothing.
+    q, k, v, do = _rand(33, 1, 2, 1, 8)
+    v = fa_inputs.bf16_to_f32(fa_inputs.bf16_bits(v))
+    a = oracle_lib.attention_bwd(q, k, v, do, False, 0.5)
+    b = oracle_lib.attention_bwd(q, k, v, do, False, 0.5, o_storage="bf16")
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)

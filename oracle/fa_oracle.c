@@ -38,9 +38,10 @@
  * rounds it to fp32 before D is formed.  Nothing else changes.
  *
  * All inputs are float64 arrays in [B, H, N, d] row-major layout (the caller
- * converts bf16 / fp32 inputs exactly).  Work is spread over (b, h) heads or
- * sampled rows with OpenMP; every head or row is computed on its own, so the
- * thread count never changes a result.
+ * converts bf16 / fp32 inputs exactly).  Work is spread over query rows (and,
+ * in the backward, over the rows of each output) with OpenMP; every output
+ * element is one sum in a fixed order, so the thread count never changes a
+ * result.
  *
  * Return value of every entry point: 0 on success, -1 on a bad argument,
  * -2 when a scratch allocation fails.
@@ -103,7 +104,7 @@ int oracle_fwd(const double* q, const double* k, const double* v,
                int64_t B, int64_t H, int64_t N, int64_t Nk, int64_t d, int causal,
                double scale, double* o, double* lse) {
     if (!q || !k || !v || !o || !lse || bad_shape(B, H, N, d) || Nk < 1) return -1;
-    int64_t BH = B * H;
+    int64_t rows = B * H * N;
     int failed = 0;
 #pragma omp parallel
     {
@@ -112,15 +113,12 @@ int oracle_fwd(const double* q, const double* k, const double* v,
 #pragma omp atomic write
             failed = 1;
         }
-#pragma omp for schedule(dynamic, 1)
-        for (int64_t bh = 0; bh < BH; ++bh) {
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; ++r) {
             if (!srow) continue;
-            const double* qh = q + bh * N * d;
-            const double* kh = k + bh * Nk * d;
-            const double* vh = v + bh * Nk * d;
-            for (int64_t i = 0; i < N; ++i)
-                attention_row(qh + i * d, kh, vh, i, Nk, d, causal, scale, srow,
-                              o + (bh * N + i) * d, lse + bh * N + i);
+            int64_t bh = r / N, i = r % N;
+            attention_row(q + r * d, k + bh * Nk * d, v + bh * Nk * d, i, Nk, d, causal, scale,
+                          srow, o + r * d, lse + r);
         }
         free(srow);
     }
@@ -194,7 +192,10 @@ static double stored_output(double x, int o_storage) {
 }
 
 /* Backward of one head with explicit N x N matrices.  All pointers are the
- * head's own [N, d] (or [N]) slices.  Scratch: 2 N^2 + N d doubles. */
+ * head's own [N, d] (or [N]) slices.  Scratch: 2 N^2 + N d doubles.  Each
+ * loop below is spread over threads by output row; every output element is
+ * still one sum in a fixed order, so the result does not depend on the
+ * thread count. */
 static int backward_head(const double* qh, const double* kh, const double* vh,
                          const double* doh, int64_t N, int64_t d, int causal, double scale,
                          int o_storage, double* dqh, double* dkh, double* dvh, double* dh) {
@@ -208,11 +209,13 @@ static int backward_head(const double* qh, const double* kh, const double* vh,
         return -2;
     }
     /* Forward again, keeping P and O (FP64). */
+#pragma omp parallel for schedule(dynamic, 8)
     for (int64_t i = 0; i < N; ++i) {
         double lse;
         attention_row(qh + i * d, kh, vh, i, N, d, causal, scale, P + i * N, O + i * d, &lse);
     }
     /* dV = P^T dO */
+#pragma omp parallel for schedule(dynamic, 8)
     for (int64_t j = 0; j < N; ++j)
         for (int64_t c = 0; c < d; ++c) {
             double acc = 0.0;
@@ -220,6 +223,7 @@ static int backward_head(const double* qh, const double* kh, const double* vh,
             dvh[j * d + c] = acc;
         }
     /* D_i = dO_i . O_i, then dS = P o (dP - D), dP_ij = dO_i . V_j */
+#pragma omp parallel for schedule(dynamic, 8)
     for (int64_t i = 0; i < N; ++i) {
         double Di = 0.0;
         for (int64_t c = 0; c < d; ++c) Di += doh[i * d + c] * stored_output(O[i * d + c], o_storage);
@@ -231,6 +235,7 @@ static int backward_head(const double* qh, const double* kh, const double* vh,
         }
     }
     /* dQ = scale dS K */
+#pragma omp parallel for schedule(dynamic, 8)
     for (int64_t i = 0; i < N; ++i)
         for (int64_t c = 0; c < d; ++c) {
             double acc = 0.0;
@@ -238,6 +243,7 @@ static int backward_head(const double* qh, const double* kh, const double* vh,
             dqh[i * d + c] = scale * acc;
         }
     /* dK = scale dS^T Q */
+#pragma omp parallel for schedule(dynamic, 8)
     for (int64_t j = 0; j < N; ++j)
         for (int64_t c = 0; c < d; ++c) {
             double acc = 0.0;
@@ -265,18 +271,14 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
     if (heads)
         for (int64_t s = 0; s < n; ++s)
             if (heads[s] < 0 || heads[s] >= B * H) return -1;
-    int failed = 0;
-#pragma omp parallel for schedule(dynamic, 1)
+    /* Heads one after the other; the threads work inside each head. */
     for (int64_t s = 0; s < n; ++s) {
         int64_t bh = heads ? heads[s] : s;
         int64_t off = bh * N * d;
         int rc = backward_head(q + off, k + off, v + off, dO + off, N, d, causal, scale,
                                o_storage, dq + s * N * d, dk + s * N * d, dv + s * N * d,
                                dvec ? dvec + s * N : NULL);
-        if (rc) {
-#pragma omp atomic write
-            failed = rc;
-        }
+        if (rc) return rc;
     }
-    return failed;
+    return 0;
 }

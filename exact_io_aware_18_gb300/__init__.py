@@ -1,0 +1,63 @@
+"""Exact IO-aware attention for GB300 (sm_103a): forward and backward.
+
+The compute lives in libfa.so (hand-written CUDA: tcgen05 tensor cores, TMEM
+accumulators, TMA copies) behind the C ABI of ``include/fa.h``; this package
+is its thin Python binding.  PyTorch only supplies device memory and streams.
+
+    from exact_io_aware_18_gb300 import attention_fwd, attention_bwd
+    o, lse = attention_fwd(q, k, v, causal=True)           # bf16 [B,H,N,d]
+    dq, dk, dv = attention_bwd(q, k, v, o, do, lse, causal=True)
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from ._lib import (FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT, FA_ERR_INVALID_ARG, FA_ERR_MISALIGNED,
+                   FA_ERR_NO_MEMORY, FA_ERR_UNSUPPORTED, FA_OK, FaError, error_string, fa_bwd,
+                   fa_bwd_dkdv, fa_bwd_f32, fa_bwd_preprocess, fa_bwd_workspace_bytes,
+                   fa_device_status, fa_fwd, fa_fwd_f32, fa_selftest_wait_timeout,
+                   fa_set_wait_timeout_ns, lib_path, load)
+
+__all__ = [
+    "attention_fwd", "attention_bwd", "fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv",
+    "fa_bwd_workspace_bytes", "fa_fwd_f32", "fa_bwd_f32", "fa_device_status",
+    "fa_set_wait_timeout_ns", "fa_selftest_wait_timeout", "FaError", "error_string", "load",
+    "lib_path", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
+    "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_NO_MEMORY",
+]
+
+
+def default_scale(d: int) -> float:
+    """1/sqrt(d) rounded to the float the C ABI receives."""
+    return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+
+
+def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocates O and LSE and runs fa_fwd (bf16) or fa_fwd_f32 (fp32)."""
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if q.dtype == torch.float32:
+        fa_fwd_f32(q, k, v, o, lse, causal, scale, stream)
+    else:
+        fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
+                  workspace=None, stream=None):
+    """Allocates FP32 dQ, dK, dV and runs fa_bwd (bf16) or fa_bwd_f32 (fp32)."""
+    d = q.shape[-1]
+    scale = default_scale(d) if scale is None else scale
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    if q.dtype == torch.float32:
+        fa_bwd_f32(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream)
+    else:
+        fa_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream)
+    return dq, dk, dv

@@ -1,0 +1,214 @@
+"""ctypes binding of libfa.so: the C-ABI calls of include/fa.h under the same names.
+
+Argument marshalling only: each function checks that it was handed CUDA
+tensors of the right dtype and layout, reads their pointers and sizes, and
+calls the library on the current (or given) stream.  Every numeric step runs
+in the library's kernels; there is no fallback of any kind, and importing the
+binding fails loudly when libfa.so has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_MISALIGNED = -3
+FA_ERR_CUDA = -4
+FA_ERR_DEVICE_TIMEOUT = -5
+FA_ERR_NO_MEMORY = -6
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_bwd_workspace_bytes": ([_i, _i, _i, _i], _sz),
+    "fa_bwd": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _sz, _vp], _i),
+    "fa_bwd_preprocess": ([_vp] * 6 + [_i, _i, _i, _i, _vp], _i),
+    "fa_bwd_dkdv": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_fwd_f32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_bwd_f32": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _sz, _vp], _i),
+    "fa_error_string": ([_i], ctypes.c_char_p),
+    "fa_device_status": ([_i], _i),
+    "fa_set_wait_timeout_ns": ([ctypes.c_ulonglong], None),
+    "fa_selftest_wait_timeout": ([ctypes.c_ulonglong, _vp], _i),
+}
+
+
+class FaError(RuntimeError):
+    """A non-zero fa_status returned by the library."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {error_string(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """The loaded libfa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it first "
+                              "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def error_string(status: int) -> str:
+    return load().fa_error_string(int(status)).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != FA_OK:
+        raise FaError(rc, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _bhnd(q: torch.Tensor):
+    if q.dim() != 4:
+        raise ValueError("tensors must be [B, H, N, d]")
+    return tuple(int(x) for x in q.shape)
+
+
+def _expect(t: torch.Tensor, name: str, dtype, shape) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ----------------------------------------------------------------- BF16 path
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """O, LSE of exact attention (bf16 q/k/v/o, fp32 lse) into o and lse."""
+    B, H, N, d = _bhnd(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _expect(t, name, torch.bfloat16, (B, H, N, d))
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    _check(load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                         int(bool(causal)), float(scale), _stream(stream)), "fa_fwd")
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_bytes(int(B), int(H), int(N), int(d)))
+
+
+def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, workspace=None,
+           stream=None) -> None:
+    """dQ, dK, dV (fp32) of exact attention; workspace None lets the library allocate."""
+    B, H, N, d = _bhnd(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _expect(t, name, torch.bfloat16, (B, H, N, d))
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _expect(t, name, torch.float32, (B, H, N, d))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale),
+                         _ptr(workspace), ws_bytes, _stream(stream)), "fa_bwd")
+
+
+def fa_bwd_preprocess(o, do, lse, delta_ws, lse2_ws, dq, stream=None) -> None:
+    """D = rowsum(dO o O) and LSE*log2(e) into padded [B*H, roundup(N,128)] vectors; dq = 0."""
+    B, H, N, d = _bhnd(o)
+    n_pad = (N + 127) // 128 * 128
+    _expect(o, "o", torch.bfloat16, (B, H, N, d))
+    _expect(do, "do", torch.bfloat16, (B, H, N, d))
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    _expect(delta_ws, "delta_ws", torch.float32, (B * H, n_pad))
+    _expect(lse2_ws, "lse2_ws", torch.float32, (B * H, n_pad))
+    _expect(dq, "dq", torch.float32, (B, H, N, d))
+    _check(load().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), _ptr(delta_ws), _ptr(lse2_ws),
+                                    _ptr(dq), B, H, N, d, _stream(stream)), "fa_bwd_preprocess")
+
+
+def fa_bwd_dkdv(q, k, v, do, delta_ws, lse2_ws, dq, dk, dv, causal: bool, scale: float,
+                stream=None) -> None:
+    """dK, dV and the dQ accumulation, after fa_bwd_preprocess."""
+    B, H, N, d = _bhnd(q)
+    n_pad = (N + 127) // 128 * 128
+    for name, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+        _expect(t, name, torch.bfloat16, (B, H, N, d))
+    _expect(delta_ws, "delta_ws", torch.float32, (B * H, n_pad))
+    _expect(lse2_ws, "lse2_ws", torch.float32, (B * H, n_pad))
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _expect(t, name, torch.float32, (B, H, N, d))
+    _check(load().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(delta_ws), _ptr(lse2_ws),
+                              _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)),
+                              float(scale), _stream(stream)), "fa_bwd_dkdv")
+
+
+# ----------------------------------------------------------------- FP32 path
+
+def fa_fwd_f32(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    B, H, N, d = _bhnd(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _expect(t, name, torch.float32, (B, H, N, d))
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    _check(load().fa_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                             int(bool(causal)), float(scale), _stream(stream)), "fa_fwd_f32")
+
+
+def fa_bwd_f32(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, workspace=None,
+               stream=None) -> None:
+    B, H, N, d = _bhnd(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk),
+                    ("dv", dv)):
+        _expect(t, name, torch.float32, (B, H, N, d))
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().fa_bwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                             _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale),
+                             _ptr(workspace), ws_bytes, _stream(stream)), "fa_bwd_f32")
+
+
+# ----------------------------------------------------------------- status
+
+def fa_device_status(clear: bool = False) -> int:
+    return int(load().fa_device_status(int(bool(clear))))
+
+
+def fa_set_wait_timeout_ns(ns: int) -> None:
+    load().fa_set_wait_timeout_ns(int(ns))
+
+
+def fa_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
+    return int(load().fa_selftest_wait_timeout(int(timeout_ns), _stream(stream)))

@@ -1,0 +1,268 @@
+// fa_api.cu - the C ABI of libfa.so (declared in include/fa.h): argument
+// checks, TMA tensor-map encoding, workspace handling and kernel dispatch.
+// Nothing here computes attention; every numeric step runs in the kernels.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+// Device status word: kernels OR kStatusTimeout into it when a bounded wait
+// gives up.  One copy per device (a __device__ variable is per context).
+__device__ unsigned int g_fa_status;
+
+std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_mutex;
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeFn g_encode = nullptr;
+
+int status_ptr(unsigned int** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return FA_OK;
+}
+
+int get_encode(EncodeFn* out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return FA_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeFn>(fn);
+    }
+    *out = g_encode;
+    return FA_OK;
+}
+
+// [B*H, N, d] bf16 viewed as (d, N, B*H); 128-row x 64-column boxes (128 bytes
+// wide, the 128-byte swizzle span).  Rows past N read as zero, stores past N
+// are dropped.
+int make_map_bf16(CUtensorMap* map, const void* ptr, int d, int N, long long BH) {
+    EncodeFn enc;
+    if (int rc = get_encode(&enc)) return rc;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int B, int H, int N, int d, float scale) {
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;
+    const long long tiles = (static_cast<long long>(N) + 127) / 128;
+    if (tiles * B * H > (1ll << 31) - 1) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ptrs) {
+    for (const void* p : ptrs)
+        if (!p) return FA_ERR_INVALID_ARG;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return FA_ERR_MISALIGNED;
+    return FA_OK;
+}
+
+long long n_pad_of(int N) { return (static_cast<long long>(N) + 127) / 128 * 128; }
+
+int launch_rc(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_error_string(int status) {
+    switch (status) {
+        case FA_OK: return "ok";
+        case FA_ERR_INVALID_ARG: return "invalid argument";
+        case FA_ERR_UNSUPPORTED: return "unsupported size or head dimension";
+        case FA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case FA_ERR_CUDA: return "CUDA error";
+        case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+        case FA_ERR_NO_MEMORY: return "workspace too small or allocation failed";
+        default: return "unknown status";
+    }
+}
+
+void fa_set_wait_timeout_ns(unsigned long long ns) {
+    g_timeout_ns.store(ns < 1000000ull ? 1000000ull : ns);
+}
+
+int fa_device_status(int clear) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_fa_status, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(zero)) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    return word ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, int causal, float scale, void* stream) {
+    if (int rc = check_ptrs({q, k, v, o, lse})) return rc;
+    if (int rc = check_shape(B, H, N, d, scale)) return rc;
+    unsigned int* status;
+    if (int rc = status_ptr(&status)) return rc;
+    const long long BH = static_cast<long long>(B) * H;
+    CUtensorMap tq, tk, tv, to;
+    if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&to, o, d, N, BH)) return rc;
+    fa::FwdArgs a{&tq, &tk, &tv, &to, lse, B, H, N, d, causal ? 1 : 0,
+                  scale * 1.4426950408889634f, status, g_timeout_ns.load()};
+    return launch_rc(fa::launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+    (void)d;
+    if (B < 1 || H < 1 || N < 1) return 0;
+    return static_cast<size_t>(2) * static_cast<size_t>(B) * static_cast<size_t>(H) *
+           static_cast<size_t>(n_pad_of(N)) * sizeof(float);
+}
+
+int fa_bwd_preprocess(const void* o, const void* do_, const float* lse, float* delta_ws,
+                      float* lse2_ws, float* dq, int B, int H, int N, int d, void* stream) {
+    if (int rc = check_ptrs({o, do_, lse, delta_ws, lse2_ws, dq})) return rc;
+    if (int rc = check_shape(B, H, N, d, 1.f)) return rc;
+    fa::BwdPreArgs a{o, do_, lse, delta_ws, lse2_ws, dq, B * H, N, d,
+                     static_cast<int>(n_pad_of(N))};
+    return launch_rc(fa::launch_bwd_pre_bf16(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
+                const float* delta_ws, const float* lse2_ws, float* dq, float* dk, float* dv,
+                int B, int H, int N, int d, int causal, float scale, void* stream) {
+    if (int rc = check_ptrs({q, k, v, do_, delta_ws, lse2_ws, dq, dk, dv})) return rc;
+    if (int rc = check_shape(B, H, N, d, scale)) return rc;
+    unsigned int* status;
+    if (int rc = status_ptr(&status)) return rc;
+    const long long BH = static_cast<long long>(B) * H;
+    CUtensorMap tq, tk, tv, tdo;
+    if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
+    fa::BwdArgs a{&tq, &tk, &tv, &tdo, delta_ws, lse2_ws, dq, dk, dv, B, H, N, d,
+                  static_cast<int>(n_pad_of(N)), causal ? 1 : 0, scale,
+                  scale * 1.4426950408889634f, status, g_timeout_ns.load()};
+    return launch_rc(fa::launch_bwd_dkdv_bf16(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_,
+           const float* lse, float* dq, float* dk, float* dv, int B, int H, int N, int d,
+           int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+    if (int rc = check_ptrs({q, k, v, o, do_, lse, dq, dk, dv})) return rc;
+    if (int rc = check_shape(B, H, N, d, scale)) return rc;
+    const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* ws = workspace;
+    if (ws) {
+        if (!aligned16(ws)) return FA_ERR_MISALIGNED;
+        if (workspace_bytes < need) return FA_ERR_NO_MEMORY;
+    } else if (cudaMallocAsync(&ws, need, s) != cudaSuccess) {
+        return FA_ERR_NO_MEMORY;
+    }
+    float* delta = static_cast<float*>(ws);
+    float* lse2 = delta + static_cast<size_t>(B) * H * n_pad_of(N);
+    int rc = fa_bwd_preprocess(o, do_, lse, delta, lse2, dq, B, H, N, d, stream);
+    if (rc == FA_OK)
+        rc = fa_bwd_dkdv(q, k, v, do_, delta, lse2, dq, dk, dv, B, H, N, d, causal, scale,
+                         stream);
+    if (!workspace && cudaFreeAsync(ws, s) != cudaSuccess && rc == FA_OK) rc = FA_ERR_CUDA;
+    return rc;
+}
+
+int fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+               int H, int N, int d, int causal, float scale, void* stream) {
+    if (int rc = check_ptrs({q, k, v, o, lse})) return rc;
+    if (int rc = check_shape(B, H, N, d, scale)) return rc;
+    if (static_cast<long long>(B) * H > 65535) return FA_ERR_UNSUPPORTED;
+    fa::F32Args a{};
+    a.q = q; a.k = k; a.v = v; a.out_o = o; a.out_lse = lse;
+    a.B = B; a.H = H; a.N = N; a.d = d; a.causal = causal ? 1 : 0; a.scale = scale;
+    return launch_rc(fa::launch_fwd_f32(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_f32(const float* q, const float* k, const float* v, const float* o, const float* do_,
+               const float* lse, float* dq, float* dk, float* dv, int B, int H, int N, int d,
+               int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+    if (int rc = check_ptrs({q, k, v, o, do_, lse, dq, dk, dv})) return rc;
+    if (int rc = check_shape(B, H, N, d, scale)) return rc;
+    if (static_cast<long long>(B) * H > 65535) return FA_ERR_UNSUPPORTED;
+    const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* ws = workspace;
+    if (ws) {
+        if (!aligned16(ws)) return FA_ERR_MISALIGNED;
+        if (workspace_bytes < need) return FA_ERR_NO_MEMORY;
+    } else if (cudaMallocAsync(&ws, need, s) != cudaSuccess) {
+        return FA_ERR_NO_MEMORY;
+    }
+    fa::F32Args a{};
+    a.q = q; a.k = k; a.v = v; a.o = o; a.dO = do_; a.lse = lse;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.delta = static_cast<float*>(ws);
+    a.B = B; a.H = H; a.N = N; a.d = d; a.causal = causal ? 1 : 0; a.scale = scale;
+    int rc = launch_rc(fa::launch_bwd_f32(a, s));
+    if (!workspace && cudaFreeAsync(ws, s) != cudaSuccess && rc == FA_OK) rc = FA_ERR_CUDA;
+    return rc;
+}
+
+int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* word = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&word), sizeof(unsigned int), s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    int rc = FA_OK;
+    unsigned int host = 0;
+    if (cudaMemsetAsync(word, 0, sizeof(unsigned int), s) != cudaSuccess ||
+        fa::launch_wait_timeout_selftest(word, timeout_ns < 1000ull ? 1000ull : timeout_ns, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(&host, word, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        rc = FA_ERR_CUDA;
+    cudaFreeAsync(word, s);
+    cudaStreamSynchronize(s);
+    if (rc != FA_OK) return rc;
+    return host ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+}  // extern "C"

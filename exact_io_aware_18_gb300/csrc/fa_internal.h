@@ -1,0 +1,90 @@
+// fa_internal.h - launch descriptors shared between the C-ABI layer
+// (fa_api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Forward (BF16).  Tensor maps view Q, K, V, O as 3-D arrays
+// (d, N, B*H) of bf16 with 128 x 64 boxes and 128-byte swizzle.
+struct FwdArgs {
+    const CUtensorMap* tm_q;
+    const CUtensorMap* tm_k;
+    const CUtensorMap* tm_v;
+    const CUtensorMap* tm_o;
+    float* lse;
+    int B, H, N, d;
+    int causal;
+    float scale_log2;  // scale * log2(e)
+    unsigned int* status;
+    unsigned long long timeout_ns;
+};
+
+cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);
+
+// Backward preprocess (BF16): D and base-2 LSE into padded [B*H, n_pad]
+// vectors, zero dq.
+struct BwdPreArgs {
+    const void* o;
+    const void* dO;
+    const float* lse;
+    float* delta;
+    float* lse2;
+    float* dq;
+    int BH, N, d, n_pad;
+};
+
+cudaError_t launch_bwd_pre_bf16(const BwdPreArgs& a, cudaStream_t stream);
+
+// Backward dK/dV + dQ (BF16).  Tensor maps as for the forward.
+struct BwdArgs {
+    const CUtensorMap* tm_q;
+    const CUtensorMap* tm_k;
+    const CUtensorMap* tm_v;
+    const CUtensorMap* tm_do;
+    const float* delta;
+    const float* lse2;
+    float* dq;
+    float* dk;
+    float* dv;
+    int B, H, N, d, n_pad;
+    int causal;
+    float scale;       // multiplies dS (dQ = dS K, dK = dS^T Q with dS scaled)
+    float scale_log2;  // scale * log2(e), for recomputing P
+    unsigned int* status;
+    unsigned long long timeout_ns;
+};
+
+cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t stream);
+
+// FP32 SIMT twins.
+struct F32Args {
+    const float* q;
+    const float* k;
+    const float* v;
+    const float* o;
+    const float* dO;
+    const float* lse;
+    float* out_o;
+    float* out_lse;
+    float* dq;
+    float* dk;
+    float* dv;
+    float* delta;
+    int B, H, N, d;
+    int causal;
+    float scale;
+};
+
+cudaError_t launch_fwd_f32(const F32Args& a, cudaStream_t stream);
+cudaError_t launch_bwd_f32(const F32Args& a, cudaStream_t stream);
+
+// Failure-detection self-test kernel (waits on a barrier nobody arrives at).
+cudaError_t launch_wait_timeout_selftest(unsigned int* status, unsigned long long timeout_ns,
+                                         cudaStream_t stream);
+
+}  // namespace fa

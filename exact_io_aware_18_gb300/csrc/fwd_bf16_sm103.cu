@@ -1,0 +1,373 @@
+// fwd_bf16_sm103.cu - exact attention forward, BF16 in / FP32 accumulate,
+// tcgen05 + TMEM + TMA on sm_103a.
+//
+// Method.  The online softmax of "LLM part 06: FlashAttention - GPU SRAM,
+// tiling and online softmax" (section 2): each query row keeps a running max m
+// and running sum l while key blocks stream past, and the output accumulator
+// is rescaled by exp(m_old - m_new) whenever the max moves.  Loop order and
+// parallelism follow "FlashAttention scaling, multi-GPU training and weight
+// quantization" (section 1): one CTA per 128-row Q tile of one (batch, head),
+// the K/V tiles in the inner loop, TMA copies issued by a producer warp, and
+// the division by l deferred to the end ("FlashAttention-2", technical
+// architecture, improvement 1).
+//
+// GB300 mapping (one CTA per SM, 192 threads):
+//   warp 0      TMA producer: Q tile once, then K_j and V_j into an NS-deep
+//               shared-memory ring (128-byte swizzle, 64-column boxes).
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
+//               score buffers, then O += P_{j-1} V_{j-1} with P read straight
+//               from TMEM, so the tensor core works on S_{j+1} while the
+//               softmax warps work on S_j.
+//   warps 2..5  softmax: thread r owns query row r (TMEM lane r): loads its
+//               row of S, masks, updates m and l, writes P as BF16 over the
+//               first half of the same TMEM columns, and rescales the O
+//               accumulator only when its max grew by more than 2^8 (the
+//               final O / l and LSE use the same stale max, so the result is
+//               unchanged).  Epilogue: O / l to BF16 through shared memory and
+//               a TMA store; LSE = ln 2 * (m + log2 l).
+//
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+d).  All waits are
+// bounded (see sm103_primitives.cuh).
+#include "fa_internal.h"
+#include "sm103_primitives.cuh"
+
+namespace fa {
+namespace {
+
+template <int D>
+struct FwdCfg {
+    static constexpr int BM = 128;                    // query rows per CTA
+    static constexpr int BN = 128;                    // keys per K/V tile
+    static constexpr int KB = D / 64;                 // 64-column (128-byte) boxes per row
+    static constexpr int BOX_BYTES = 128 * 64 * 2;    // one 128 x 64 bf16 box
+    static constexpr int TILE_BYTES = KB * BOX_BYTES; // one 128 x D bf16 tile
+    static constexpr int NS = (D == 128) ? 2 : 4;     // K/V ring depth
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
+    static constexpr int BAR_BYTES = 512;
+    static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
+    static constexpr int THREADS = 192;
+};
+
+// Barrier slots (8 bytes each) inside the barrier area.
+template <int NS>
+struct FwdBars {
+    static constexpr int Q_FULL = 0;
+    static constexpr int K_FULL = 1;
+    static constexpr int V_FULL = K_FULL + NS;
+    static constexpr int K_EMPTY = V_FULL + NS;
+    static constexpr int V_EMPTY = K_EMPTY + NS;
+    static constexpr int S_FULL = V_EMPTY + NS;  // 2
+    static constexpr int P_FULL = S_FULL + 2;    // 2
+    static constexpr int O_FULL = P_FULL + 2;
+    static constexpr int DONE = O_FULL + 1;
+    static constexpr int COUNT = DONE + 1;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o, float* __restrict__ lse, int N,
+                    int BH, int n_tiles, float scale_log2, unsigned int* status,
+                    unsigned long long timeout_ns) {
+    using C = FwdCfg<D>;
+    using Bar = FwdBars<C::NS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t s_q = s_base + C::OFF_Q;
+    const uint32_t s_k = s_base + C::OFF_K;
+    const uint32_t s_v = s_base + C::OFF_V;
+    const uint32_t s_bar = s_base + C::OFF_BAR;
+    auto bar = [&](int slot) -> uint32_t { return s_bar + 8u * static_cast<uint32_t>(slot); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * Bar::COUNT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    // Heavy tiles first: with a causal mask the last Q tile sees the most keys.
+    const long long lin = blockIdx.x + static_cast<long long>(gridDim.x) *
+                                           (blockIdx.y + static_cast<long long>(gridDim.y) *
+                                                             blockIdx.z);
+    const int qt = n_tiles - 1 - static_cast<int>(lin / BH);
+    const int bh = static_cast<int>(lin % BH);
+    const int n_kv = CAUSAL ? qt + 1 : n_tiles;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(Bar::Q_FULL), 1);
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(bar(Bar::K_FULL + s), 1);
+            mbar_init(bar(Bar::V_FULL + s), 1);
+            mbar_init(bar(Bar::K_EMPTY + s), 1);
+            mbar_init(bar(Bar::V_EMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(Bar::S_FULL + b), 1);
+            mbar_init(bar(Bar::P_FULL + b), 4);
+        }
+        mbar_init(bar(Bar::O_FULL), 1);
+        mbar_init(bar(Bar::DONE), 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_o);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const WaitCtx wc{status, timeout_ns, abort_flag};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(Bar::Q_FULL), C::TILE_BYTES);
+            for (int kb = 0; kb < C::KB; ++kb)
+                tma_load_3d(s_q + kb * C::BOX_BYTES, &tm_q, bar(Bar::Q_FULL), kb * 64,
+                            qt * C::BM, bh);
+            int issued = 0;
+            bool ok = true;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int st = j % C::NS;
+                const int use = j / C::NS;
+                if (use > 0) ok = mbar_wait(bar(Bar::K_EMPTY + st), (use - 1) & 1, wc);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(Bar::K_FULL + st), C::TILE_BYTES);
+                for (int kb = 0; kb < C::KB; ++kb)
+                    tma_load_3d(s_k + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_k,
+                                bar(Bar::K_FULL + st), kb * 64, j * C::BN, bh);
+                if (use > 0) ok = mbar_wait(bar(Bar::V_EMPTY + st), (use - 1) & 1, wc);
+                if (!ok) {
+                    // K_j is in flight: wait for it before leaving.
+                    mbar_wait_drain(bar(Bar::K_FULL + st), use & 1, timeout_ns);
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(Bar::V_FULL + st), C::TILE_BYTES);
+                for (int kb = 0; kb < C::KB; ++kb)
+                    tma_load_3d(s_v + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_v,
+                                bar(Bar::V_FULL + st), kb * 64, j * C::BN, bh);
+                issued = j + 1;
+            }
+            // Drain: no copy may still be landing when the CTA exits.
+            mbar_wait_drain(bar(Bar::Q_FULL), 0, timeout_ns);
+            for (int j = (issued > C::NS ? issued - C::NS : 0); j < issued; ++j) {
+                mbar_wait_drain(bar(Bar::K_FULL + j % C::NS), (j / C::NS) & 1, timeout_ns);
+                mbar_wait_drain(bar(Bar::V_FULL + j % C::NS), (j / C::NS) & 1, timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);
+            auto issue_pv = [&](int t) -> bool {
+                const int b = t & 1;
+                const int st = t % C::NS;
+                if (!mbar_wait(bar(Bar::P_FULL + b), (t >> 1) & 1, wc)) return false;
+                if (!mbar_wait(bar(Bar::V_FULL + st), (t / C::NS) & 1, wc)) return false;
+                tc_fence_after();
+                const uint32_t a_tmem = tmem + (b ? C::COL_S1 : C::COL_S0);
+                const uint32_t v_tile = s_v + st * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk) {
+                    // V as an MN-major B operand: 16 keys = 2 atoms of 8 rows.
+                    const uint64_t bd = smem_desc_sw128(v_tile + kk * 2048, C::BOX_BYTES, 1024);
+                    mma_ts(tmem + C::COL_O, a_tmem + kk * 8, bd, id_pv, (t > 0 || kk > 0));
+                }
+                tc_commit(bar(Bar::V_EMPTY + st));
+                tc_commit(bar(Bar::O_FULL));
+                return true;
+            };
+            bool ok = mbar_wait(bar(Bar::Q_FULL), 0, wc);
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int st = j % C::NS;
+                const int b = j & 1;
+                ok = mbar_wait(bar(Bar::K_FULL + st), (j / C::NS) & 1, wc);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t k_tile = s_k + st * C::TILE_BYTES;
+                const uint32_t d_tmem = tmem + (b ? C::COL_S1 : C::COL_S0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                    const uint64_t ad = smem_desc_sw128(s_q + koff, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(k_tile + koff, 16, 1024);
+                    mma_ss(d_tmem, ad, bd, id_s, kk > 0);
+                }
+                tc_commit(bar(Bar::S_FULL + b));
+                tc_commit(bar(Bar::K_EMPTY + st));
+                if (j > 0) ok = issue_pv(j - 1);
+            }
+            if (ok) issue_pv(n_kv - 1);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int wq = warp & 3;             // TMEM lane quarter of this warp
+        const int row = wq * 32 + lane;      // row inside the Q tile
+        const int grow = qt * C::BM + row;   // query index inside the head
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        float m_run = -INFINITY;  // running max, base-2 units of scale * S
+        float l_run = 0.f;        // running sum of 2^(x - m_run)
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            const int b = j & 1;
+            const uint32_t t_s = t_lane + (b ? C::COL_S1 : C::COL_S0);
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_FULL + b), (j >> 1) & 1, wc));
+            if (!ok) break;
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(t_s + c * 32, r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
+            }
+            const int key0 = j * C::BN;
+            if ((CAUSAL && j == qt) || key0 + C::BN > N) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int key = key0 + c;
+                    if ((CAUSAL && key > grow) || key >= N) s[c] = -INFINITY;
+                }
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            const float m_tile = mx * scale_log2;
+            const bool rescale = m_tile > m_run + 8.0f;
+            float alpha = 1.f;
+            if (rescale) {
+                alpha = ex2_approx(m_run - m_tile);
+                m_run = m_tile;
+            }
+            const float neg_m = -m_run;
+            float sum = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * e], scale_log2, neg_m));
+                    const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * e + 1], scale_log2, neg_m));
+                    sum += p0 + p1;
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(t_s + h * 32, pk);
+            }
+            l_run = l_run * alpha + sum;
+            tmem_st_wait();
+            if (j > 0) {
+                // O holds the sum up to PV_{j-1}; it must be complete before a rescale
+                // and before P_j is released.
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::O_FULL), (j - 1) & 1, wc));
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(t_lane + C::COL_O + c * 32, r);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        tmem_st32(t_lane + C::COL_O + c * 32, r);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Bar::P_FULL + b));
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::O_FULL), (n_kv - 1) & 1, wc));
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = 1.f / l_run;
+            if (grow < N) lse[static_cast<long long>(bh) * N + grow] =
+                              (m_run + lg2_approx(l_run)) * 0.69314718055994531f;
+            // O / l -> bf16 into the (now free) Q buffer, in the TMA box layout.
+            uint8_t* stage = smem + C::OFF_Q;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(t_lane + C::COL_O + c * 32, r);
+                const int box = c >> 1;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(r[8 * u + 0]) * inv_l,
+                                      __uint_as_float(r[8 * u + 1]) * inv_l);
+                    w.y = pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv_l,
+                                      __uint_as_float(r[8 * u + 3]) * inv_l);
+                    w.z = pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv_l,
+                                      __uint_as_float(r[8 * u + 5]) * inv_l);
+                    w.w = pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv_l,
+                                      __uint_as_float(r[8 * u + 7]) * inv_l);
+                    const int chunk = ((c & 1) * 4 + u) ^ (row & 7);
+                    *reinterpret_cast<uint4*>(stage + box * C::BOX_BYTES + row * 128 +
+                                              chunk * 16) = w;
+                }
+            }
+            fence_async_smem();
+        }
+        named_bar_sync(1, 128);
+        if (ok && threadIdx.x == 64 && !*abort_flag) {
+            for (int kb = 0; kb < C::KB; ++kb)
+                tma_store_3d(&tm_o, s_q + kb * C::BOX_BYTES, kb * 64, qt * C::BM, bh);
+            bulk_commit();
+            bulk_wait_all();
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    __syncthreads();
+    if (warp == 1) {
+        if (lane == 0) {
+            tc_commit(bar(Bar::DONE));
+            mbar_wait_drain(bar(Bar::DONE), 0, timeout_ns);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+    using C = FwdCfg<D>;
+    auto kern = fwd_bf16_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int n_tiles = (a.N + C::BM - 1) / C::BM;
+    dim3 grid(n_tiles, a.H, a.B);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse,
+                                                       a.N, a.B * a.H, n_tiles, a.scale_log2,
+                                                       a.status, a.timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream) {
+    if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream)
+                                   : launch_fwd_t<64, false>(a, stream);
+    return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,143 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) exact-attention library libfa.so.
+ *
+ * Operation.  For every batch b and head h, with S = scale * Q K^T:
+ *
+ *     O   = softmax(S [+ causal mask]) V
+ *     LSE = per-row natural-log logsumexp of the (masked) row of S
+ *
+ * (standard attention as restated in "Flash Attention: Revolutionizing
+ * Transformer Efficiency", section "Standard attention: a quick recap"), and
+ * its gradient dQ, dK, dV.  The forward is computed tile by tile with the
+ * online-softmax running max and running sum ("LLM part 06: FlashAttention -
+ * GPU SRAM, tiling and online softmax", section 2), so the N x N score matrix
+ * never reaches device memory; the backward recomputes the probabilities from
+ * the saved LSE ("Flash Attention: Revolutionizing Transformer Efficiency",
+ * section "The Flash Attention algorithm", idea 2, recomputation).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors Q, K, V, O, dO, dQ, dK, dV are [B, H, N, d] row-major and
+ *     contiguous; LSE is [B, H, N].  Queries and keys have the same length N.
+ *   - Causal (causal != 0): key j is visible to query i iff j <= i.
+ *   - scale multiplies Q K^T before the softmax; it must be finite and > 0
+ *     (the usual value is 1/sqrt(d)).
+ *   - All pointers are DEVICE pointers into memory of the current CUDA
+ *     device, owned by the caller; the library never frees them.  Every
+ *     pointer must be 16-byte aligned.
+ *   - stream is a cudaStream_t passed as void* (NULL: the legacy default
+ *     stream).  Work is enqueued on it and the call returns without waiting.
+ *   - Return value: FA_OK, or a negative fa_status.  Argument errors
+ *     (INVALID_ARG, UNSUPPORTED, MISALIGNED) are found before anything is
+ *     launched.  FA_ERR_CUDA reports a launch error.  A kernel that gives up
+ *     on a bounded wait records FA_ERR_DEVICE_TIMEOUT in the library's device
+ *     status word, read with fa_device_status().
+ *   - The library holds no state between calls other than the per-device
+ *     status word and a cached driver entry point; calls are thread-safe as
+ *     long as their buffers do not overlap.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = -1,    /* null pointer, non-positive size, bad scale  */
+    FA_ERR_UNSUPPORTED = -2,    /* head dimension or size outside what is built */
+    FA_ERR_MISALIGNED = -3,     /* a pointer is not 16-byte aligned            */
+    FA_ERR_CUDA = -4,           /* a CUDA runtime/driver call or launch failed */
+    FA_ERR_DEVICE_TIMEOUT = -5, /* a kernel gave up on a bounded wait          */
+    FA_ERR_NO_MEMORY = -6,      /* workspace too small or allocation failed    */
+} fa_status;
+
+/* Forward, BF16 inputs and output, FP32 accumulation.
+ *
+ * q, k, v : const bf16 [B,H,N,d];  o : bf16 [B,H,N,d] (written);
+ * lse     : float [B,H,N] (written), natural log.
+ * d must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).  N may be any value
+ * >= 1: the ragged last tile is masked.  B, H <= 65535.
+ *
+ * Each CTA owns one 128-row Q tile of one (b, h) and streams the 128-key
+ * K/V tiles through a shared-memory ring ("FlashAttention scaling, multi-GPU
+ * training and weight quantization", section 1: loop order with Q outside,
+ * parallelism over the sequence, asynchronous TMA copies); the 1/l
+ * normalisation is applied once at the end ("FlashAttention-2", technical
+ * architecture, improvement 1). */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/* Bytes of device workspace fa_bwd needs: two FP32 vectors per (b, h) of
+ * length N rounded up to 128 (D = rowsum(dO o O) and LSE in base 2). */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/* Backward, BF16 inputs, FP32 gradients.
+ *
+ * q, k, v, o, do_ : const bf16 [B,H,N,d]  (o and lse as written by fa_fwd);
+ * lse             : const float [B,H,N];
+ * dq, dk, dv      : float [B,H,N,d] (written; dq is zeroed then accumulated).
+ * workspace       : device buffer of at least fa_bwd_workspace_bytes() bytes,
+ *                   16-byte aligned, or NULL: the library then allocates and
+ *                   frees it on the stream (cudaMallocAsync / cudaFreeAsync).
+ *
+ * Runs fa_bwd_preprocess then fa_bwd_dkdv on the stream.  dq is reduced
+ * with FP32 atomics, so its bits may differ from run to run within rounding. */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_,
+           const float* lse, float* dq, float* dk, float* dv,
+           int B, int H, int N, int d, int causal, float scale,
+           void* workspace, size_t workspace_bytes, void* stream);
+
+/* First backward step.  delta_ws : float [B*H, roundup(N,128)] receives
+ * D_i = sum_c dO_ic O_ic (0 on padding rows); lse2_ws (same shape) receives
+ * LSE_i * log2(e) (+inf on padding rows); dq [B,H,N,d] is set to zero.
+ * Memory-bound; d must be 64 or 128. */
+int fa_bwd_preprocess(const void* o, const void* do_, const float* lse, float* delta_ws,
+                      float* lse2_ws, float* dq, int B, int H, int N, int d, void* stream);
+
+/* Second backward step.  One CTA per 128-key K/V tile of one (b, h): it keeps
+ * K, V and the dK, dV accumulators on chip and loops over the Q tiles that
+ * see those keys, recomputing P from lse2_ws, and adds each dQ tile into dq
+ * with FP32 atomics.  delta_ws / lse2_ws as written by fa_bwd_preprocess. */
+int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
+                const float* delta_ws, const float* lse2_ws, float* dq, float* dk, float* dv,
+                int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/* FP32 twins (FP32 inputs and outputs, FP32 arithmetic on CUDA cores, no
+ * TF32).  Same shapes and conventions as the BF16 calls; d is 64 or 128.
+ * fa_bwd_f32's workspace holds D: at least fa_bwd_workspace_bytes() bytes,
+ * or NULL to let the library allocate it on the stream. */
+int fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+               int B, int H, int N, int d, int causal, float scale, void* stream);
+int fa_bwd_f32(const float* q, const float* k, const float* v, const float* o,
+               const float* do_, const float* lse, float* dq, float* dk, float* dv,
+               int B, int H, int N, int d, int causal, float scale,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static description of an fa_status value (never NULL). */
+const char* fa_error_string(int status);
+
+/* Synchronises the current device, then returns FA_ERR_DEVICE_TIMEOUT if a
+ * kernel of this library has recorded a bounded-wait timeout on it since the
+ * last clear, FA_ERR_CUDA if the synchronisation itself failed, else FA_OK.
+ * clear != 0 resets the word. */
+int fa_device_status(int clear);
+
+/* Upper bound, in nanoseconds, on any single wait inside a kernel launched
+ * after this call (default 4e9).  Values below 1e6 are raised to 1e6. */
+void fa_set_wait_timeout_ns(unsigned long long ns);
+
+/* Failure-detection self-test: launches one CTA that waits on a barrier no
+ * thread ever arrives at, bounded by timeout_ns, and synchronises.  Returns
+ * FA_ERR_DEVICE_TIMEOUT when the kernel gave up and reported it (the
+ * expected outcome), FA_OK if the wait somehow completed, FA_ERR_CUDA on a
+ * CUDA error.  Does not touch the status word read by fa_device_status. */
+int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

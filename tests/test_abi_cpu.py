@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports what include/fa.h declares;
+host-side argument checks reject bad calls before anything is launched.
+None of these calls reaches a kernel, so no GPU is needed."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from exact_io_aware_18_gb300 import build
+    build.build()
+    import exact_io_aware_18_gb300 as pkg
+    pkg.load()
+    return pkg
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(fa_[a-z0-9_]+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("fa_fwd", "fa_bwd", "fa_fwd_f32", "fa_bwd_f32", "fa_bwd_workspace_bytes",
+                 "fa_error_string", "fa_device_status", "fa_bwd_preprocess", "fa_bwd_dkdv"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(fa):
+    lib = ctypes.CDLL(fa.lib_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(fa_[a-z0-9_]+)$", out, flags=re.M))
+    assert set(declared_functions()) <= exported
+
+
+def test_error_strings(fa):
+    for status in range(-6, 1):
+        assert fa.error_string(status)
+    assert fa.error_string(-99) == "unknown status"
+
+
+def test_workspace_is_linear_in_n(fa):
+    # The page on GPU SRAM and tiling notes that at N = 32000 the N x N score
+    # matrix alone is about 2 GB per head in 16-bit; the backward's workspace
+    # must stay O(N) (two FP32 vectors per head).
+    n = 32000
+    ws = fa.fa_bwd_workspace_bytes(1, 1, n, 128)
+    assert ws == 2 * 4 * ((n + 127) // 128 * 128)
+    assert ws < n * n * 2 / 1000
+    assert fa.fa_bwd_workspace_bytes(8, 16, 2048, 128) == 2 * 4 * 8 * 16 * 2048
+    assert fa.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
+
+
+def _call_fwd(lib, ptrs, B=1, H=1, N=128, d=64, causal=0, scale=0.125):
+    return lib.fa_fwd(*ptrs, B, H, N, d, causal, scale, None)
+
+
+def test_argument_checks_before_launch(fa):
+    lib = fa.load()
+    good = [0x10000 * (i + 1) for i in range(5)]  # aligned fake pointers: never dereferenced
+    assert _call_fwd(lib, [0] + good[1:]) == fa.FA_ERR_INVALID_ARG
+    assert _call_fwd(lib, [good[0] + 8] + good[1:]) == fa.FA_ERR_MISALIGNED
+    assert _call_fwd(lib, good, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert _call_fwd(lib, good, d=256) == fa.FA_ERR_UNSUPPORTED
+    assert _call_fwd(lib, good, N=0) == fa.FA_ERR_INVALID_ARG
+    assert _call_fwd(lib, good, B=-1) == fa.FA_ERR_INVALID_ARG
+    assert _call_fwd(lib, good, scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert _call_fwd(lib, good, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert _call_fwd(lib, good, scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert _call_fwd(lib, good, B=70000) == fa.FA_ERR_UNSUPPORTED
+    f32 = lib.fa_fwd_f32(0, *good[1:], 1, 1, 16, 64, 0, 0.125, None)
+    assert f32 == fa.FA_ERR_INVALID_ARG
+    bwd = lib.fa_bwd(*([0x10000] * 9), 1, 1, 16, 80, 0, 0.125, None, 0, None)
+    assert bwd == fa.FA_ERR_UNSUPPORTED
+    bwd = lib.fa_bwd(*([0x10000] * 8 + [0x10004]), 1, 1, 16, 64, 0, 0.125, None, 0, None)
+    assert bwd == fa.FA_ERR_MISALIGNED
+    bwd = lib.fa_bwd(*([0x10000] * 9), 1, 1, 16, 64, 0, 0.125, 0x20000, 16, None)
+    assert bwd == fa.FA_ERR_NO_MEMORY
+    pre = lib.fa_bwd_preprocess(*([0x10000] * 5 + [0]), 1, 1, 16, 64, None)
+    assert pre == fa.FA_ERR_INVALID_ARG
+
+
+def test_binding_rejects_cpu_tensors(fa):
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 1, 8)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q, q, lse, False, 0.125)

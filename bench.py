@@ -1,0 +1,416 @@
+"""Throughput of the exact-attention training step on GB300.
+
+One step = the whole hot path over one batch of the training-step workload
+(bf16, B=8 H=16 N=2048 d=128, causal, scale 1/sqrt(d), seeded N(0,1) Q, K, V,
+dO): the forward (O, LSE), then the backward preprocess (D, dq = 0) and the
+dK/dV kernel with the dQ accumulation.  The metric counts 4 B H N^2 d FLOPs
+for the forward and 2.5x that for the backward, halved for the causal mask.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
+(weak scaling over independent (batch, head) work, no collective on the data
+path); the barrier and the max over ranks of the timed region stay.
+``--impl reference`` times the FP64 CPU oracle on a bounded sample of the same
+workload instead (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("attention fwd/bwd TFLOP/s (4BHN²d, causal halved) and % of GB300 BF16 tensor "
+          "peak")
+B, H, N, D, CAUSAL, SEED = 8, 16, 2048, 128, True, 4
+WORKLOAD = "training step fwd+bwd, bf16, B=8 H=16 N=2048 d=128, causal, scale=1/sqrt(d), seed 4"
+
+# DRAM traffic of one dK/dV launch at this workload, from
+# profiles/kernels_training_step_b8_h16_n2048_d128_causal.md; valid only for the kernel
+# source it was measured on (sha256 of csrc/bwd_bf16_sm103.cu).
+DKDV_TRAFFIC = {"bytes": 3018670000, "src_sha256": "8400ed945337925c60d3056fdb8c14b9996aa47240331a5d021ea1bf9151c124"}
+DKDV_SRC = os.path.join(ROOT, "exact_io_aware_18_gb300", "csrc", "bwd_bf16_sm103.cu")
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def step_flops(b=B, h=H, n=N, d=D, causal=CAUSAL):
+    fwd = 4.0 * b * h * n * n * d
+    if causal:
+        fwd /= 2
+    return fwd, 2.5 * fwd
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.samples = []  # (t, sm, max, reasons)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm, mx = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            reasons = [n for n, v in zip(self.NAMES, parts[4:8]) if v.lower() == "active"]
+            self.samples.append((time.monotonic(), sm, mx, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        used = inside
+        if len(used) < 3:  # a short timed region: take the samples nearest to it
+            used = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:5]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({r for s in used for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in used),
+                "sm_max_mhz": max(s[2] for s in used), "reasons": reasons,
+                "samples": len(used), "samples_inside_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_step_sample(x, n_heads):
+    """One oracle fwd+bwd over the first n_heads heads; returns (seconds, flops)."""
+    import oracle
+    qs = x["q"].reshape(B * H, 1, N, D)[:n_heads].reshape(1, n_heads, N, D)
+    ks = x["k"].reshape(B * H, 1, N, D)[:n_heads].reshape(1, n_heads, N, D)
+    vs = x["v"].reshape(B * H, 1, N, D)[:n_heads].reshape(1, n_heads, N, D)
+    dos = x["do"].reshape(B * H, 1, N, D)[:n_heads].reshape(1, n_heads, N, D)
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    t0 = time.perf_counter()
+    oracle.attention_fwd(qs, ks, vs, CAUSAL, scale)
+    oracle.attention_bwd(qs, ks, vs, dos, CAUSAL, scale, o_storage="bf16")
+    dt = time.perf_counter() - t0
+    f, b = step_flops(1, n_heads)
+    return dt, f + b
+
+
+def oracle_cores():
+    import oracle
+    oracle.build()
+    return oracle.num_threads()
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_io_aware_18_gb300 as fa
+    import fa_inputs
+
+    scale = fa.default_scale(D)
+    x = fa_inputs.attention_inputs(SEED + rank, B, H, N, D, "bf16")
+
+    def host_bf16(name):
+        return torch.from_numpy(x[name + "_bits"].view(np.int16)).view(torch.bfloat16)
+
+    hq, hk, hv, hdo = (host_bf16(n).pin_memory() for n in ("q", "k", "v", "do"))
+    q, k, v, do = (t.to(dev) for t in (hq, hk, hv, hdo))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq = torch.empty((B, H, N, D), dtype=torch.float32, device=dev)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    n_pad = (N + 127) // 128 * 128
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, D) // 4, dtype=torch.float32, device=dev)
+    delta = ws[:B * H * n_pad].view(B * H, n_pad)
+    lse2 = ws[B * H * n_pad:].view(B * H, n_pad)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_bwd_preprocess(o, do, lse, delta, lse2, dq, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        fa.fa_bwd_dkdv(q, k, v, do, delta, lse2, dq, dk, dv, CAUSAL, scale, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_status(clear=True) != fa.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait during warm-up")
+
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[local])
+        except ValueError:
+            pass
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.3)
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.monotonic()
+    start.record(stream)
+    for i in range(args.steps):
+        step(events[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.monotonic()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    if fa.fa_device_status(clear=True) != fa.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait in the timed region")
+
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
+    pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+    dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in events)
+
+    # End to end through the public calls: pinned host inputs in, outputs back.
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
+    hdk = torch.empty_like(hdq).pin_memory()
+    hdv = torch.empty_like(hdq).pin_memory()
+
+    def e2e_step():
+        for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+            dst.copy_(src, non_blocking=True)
+        fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream)
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, CAUSAL, scale, ws, stream)
+        for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    sampler.stop()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    f_fwd, f_bwd = step_flops()
+    ms_per_step = elapsed_ms / args.steps
+    value = world * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = f_bwd / (dkdv_ms * 1e-3) / 1e12
+    traffic = None
+    try:
+        with open(DKDV_SRC, "rb") as fsrc:
+            sha = hashlib.sha256(fsrc.read()).hexdigest()
+        if DKDV_TRAFFIC["bytes"] and DKDV_TRAFFIC["src_sha256"] == sha:
+            traffic = DKDV_TRAFFIC["bytes"]
+    except OSError:
+        pass
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # CPU baseline: the oracle as it stands on a bounded sample (whole heads).
+    cores = oracle_cores()
+    n_heads = max(1, min(B * H, cores))
+    cpu_s, cpu_flops = oracle_step_sample(x, n_heads)
+
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    pre_bytes = (2 * B * H * N * D * 2 + B * H * N * 4 + 2 * B * H * n_pad * 4
+                 + B * H * N * D * 4)
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "causal": CAUSAL,
+                   "l2": "inputs larger than L2: Q, K, V, dO are 4 x 64 MiB per step"},
+        "roofline": {"bound": "tensor", "kernel": "bwd_dkdv_bf16", "achieved": round(achieved, 2),
+                     "peak": peak, "peak_kind": f"bf16_tflops_sustained ({peak_kind})",
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic},
+        "cpu_baseline": {"value": round(cpu_flops / cpu_s / 1e12, 6), "unit": "TFLOP/s",
+                         "cores": cores, "kind": "oracle",
+                         "sample": f"{n_heads} of {B * H} heads (whole heads, fwd+bwd), "
+                                   f"{cpu_s:.1f} s"},
+        "e2e": {"value": round(world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "kernels": {
+            "fwd": {"ms": round(fwd_ms, 4), "tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
+                    "frac_of_peak": round(f_fwd / (fwd_ms * 1e-3) / 1e12 / peak, 4)},
+            "bwd_preprocess": {"ms": round(pre_ms, 4),
+                               "gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
+                               "frac_of_hbm": round(pre_bytes / (pre_ms * 1e-3) / 1e9 / hbm, 4)},
+            "bwd_dkdv": {"ms": round(dkdv_ms, 4), "tflops": round(achieved, 2)},
+            "bwd_total_tflops": round(f_bwd / ((pre_ms + dkdv_ms) * 1e-3) / 1e12, 2),
+        },
+    }
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import fa_inputs
+    cores = oracle_cores()
+    n_heads = max(1, min(B * H, cores))
+    x = fa_inputs.attention_inputs(SEED, B, H, N, D, "bf16")
+    for _ in range(args.warmup):
+        oracle_step_sample(x, n_heads)
+    total_s, total_f = 0.0, 0.0
+    for _ in range(args.steps):
+        s, f = oracle_step_sample(x, n_heads)
+        total_s += s
+        total_f += f
+    value = total_f / total_s / 1e12
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total_s / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "causal": CAUSAL,
+                   "l2": "CPU oracle"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{n_heads} of {B * H} heads per step (whole heads, fwd+bwd)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.steps < 1:
+        p.error("--steps must be at least 1")
+    if args.impl == "reference":
+        if "--steps" not in (argv or sys.argv):
+            args.steps = 5
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

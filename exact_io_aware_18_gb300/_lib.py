@@ -43,7 +43,10 @@ _SIGNATURES = {
     "fa_device_status": ([_i], _i),
     "fa_set_wait_timeout_ns": ([ctypes.c_ulonglong], None),
     "fa_selftest_wait_timeout": ([ctypes.c_ulonglong, _vp], _i),
+    "fa_bwd_noalloc": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp], _i),
 }
+
+NOALLOC_SCRATCH_BYTES = 8 << 20  # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
 
 
 class FaError(RuntimeError):
@@ -174,6 +177,28 @@ def fa_bwd_dkdv(q, k, v, do, delta_ws, lse2_ws, dq, dk, dv, causal: bool, scale:
     _check(load().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(delta_ws), _ptr(lse2_ws),
                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)),
                               float(scale), _stream(stream)), "fa_bwd_dkdv")
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float,
+                   stream=None) -> None:
+    """fa_bwd without a workspace and without any device allocation.
+
+    For callers that may not allocate device memory at call time: the D / LSE2
+    scratch is an array of NOALLOC_SCRATCH_BYTES built into the library (one
+    per GPU, kept until the process exits).  Raises FaError (FA_ERR_NO_MEMORY)
+    when the workload needs more.  The first call on a device should come
+    before any stream capture; calls that overlap on the GPU race on the
+    shared array.
+    """
+    B, H, N, d = _bhnd(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _expect(t, name, torch.bfloat16, (B, H, N, d))
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _expect(t, name, torch.float32, (B, H, N, d))
+    _check(load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)),
+                                 float(scale), _stream(stream)), "fa_bwd_noalloc")
 
 
 # ----------------------------------------------------------------- FP32 path

@@ -32,8 +32,9 @@
  *     on a bounded wait records FA_ERR_DEVICE_TIMEOUT in the library's device
  *     status word, read with fa_device_status().
  *   - The library holds no state between calls other than the per-device
- *     status word and a cached driver entry point; calls are thread-safe as
- *     long as their buffers do not overlap.
+ *     status word, a cached driver entry point and the scratch array of
+ *     fa_bwd_noalloc; calls are thread-safe as long as their buffers do not
+ *     overlap (fa_bwd_noalloc calls share one array, see there).
  */
 #ifndef FA_H
 #define FA_H
@@ -104,6 +105,28 @@ int fa_bwd_preprocess(const void* o, const void* do_, const float* lse, float* d
 int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
                 const float* delta_ws, const float* lse2_ws, float* dq, float* dk, float* dv,
                 int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/* Size of the scratch array built into the library for fa_bwd_noalloc:
+ * 8 MiB, i.e. B * H * roundup(N, 128) <= 1048576. */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/* Backward that allocates no device memory (the pages have no counterpart:
+ * this is a service to callers, not a step of the method).  For callers that
+ * cannot allocate at call time: runtimes that reserve their whole device
+ * memory budget at start-up, or code whose memory belongs to an allocator it
+ * must not bypass.  Same arguments and results as fa_bwd, minus the
+ * workspace: the D / LSE2 scratch lives in an array of
+ * FA_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that loads
+ * the library until the process exits.  Returns FA_ERR_NO_MEMORY, before
+ * launching anything, when 2 * 4 * B * H * roundup(N,128) bytes exceed it.
+ * The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the array and it keeps the last
+ * call's contents (every entry a call reads is first written by that call);
+ * calls that overlap on the GPU race on it. */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* do_,
+                   const float* lse, float* dq, float* dk, float* dv,
+                   int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /* FP32 twins (FP32 inputs and outputs, FP32 arithmetic on CUDA cores, no
  * TF32).  Same shapes and conventions as the BF16 calls; d is 64 or 128.

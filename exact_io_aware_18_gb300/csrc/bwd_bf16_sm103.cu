@@ -1,4 +1,4 @@
-// bwd_bf16_sm103.cu - attention backward, dK/dV kernel with the dQ atomics,
+// bwd_bf16_sm103.cu - attention backward, dK/dV kernel with the dQ reduction,
 // BF16 in / FP32 accumulate, tcgen05 + TMEM + TMA on sm_103a.
 //
 // Method.  The gradient of O = softmax(scale Q K^T) V with the probabilities
@@ -12,96 +12,129 @@
 // see those keys (i >= j when causal); the parallelism over key tiles of one
 // head is the sequence parallelism of "FlashAttention-2" (technical
 // architecture, improvement 2).  Each dQ_i tile is computed on the tensor
-// core and added to the FP32 dq buffer with vector atomics.
+// core and added into the FP32 dq buffer by a TMA bulk reduction.
 //
-// Roles (192 threads, one CTA per SM):
-//   warp 0      TMA producer: K_j, V_j once; per Q tile: Q_i, dO_i tiles and
-//               the 128-entry LSE2 / D vectors (bulk copies).
-//   warp 1      MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T (SS), then, once
-//               the compute warps have produced P and dS:
-//               dV += P^T dO_i (A = P^T from TMEM), dK += dS^T Q_i,
-//               dQ_i = dS K (A = dS from shared memory, read M-major).
-//   warps 2..5  thread r owns key row r (TMEM lane r): recomputes its row of
-//               P^T, forms dS^T, writes P^T (BF16) to TMEM and dS^T (BF16) to
-//               shared memory; then, as owners of query rows, read dQ_i out of
-//               TMEM and add it to dq; at the end store dK, dV (FP32).
-// TMEM columns: S^T [0,128), dP^T / dQ_i [128,256), dV [256,256+d),
-// dK [256+d, 256+2d).  Scale is folded into dS before the BF16 rounding.
+// Roles (320 threads, one CTA per SM):
+//   warp 0      TMA producer: K_j, V_j once; per Q tile, into a two-deep ring
+//               of [Q_i | dO_i] stages plus the 128-entry LSE2 / D vectors.
+//               When the compute warps have staged dQ_i (FP32) in that stage
+//               buffer, it issues the bulk reduce-add into dq, waits until the
+//               reduction has read the buffer, and reloads it with Q_{i+2}.
+//   warp 1      MMA issuer.  Tensor-pipe order, per tile t:
+//                 dP^T_t = V dO_t^T        (after dQ_{t-1} left the DP columns)
+//                 dV    += P^T_t dO_t      A = P^T in TMEM (after P_FULL)
+//                 S^T_t+1 = K Q_t+1^T      overwrites P^T_t after dV read it
+//                 dK    += dS^T_t Q_t      A = dS^T in smem (after DS_FULL)
+//                 dQ_t   = dS_t K          A = dS (M-major) -> DP columns
+//               so S^T of the next tile runs while the dS math of this one does.
+//   warps 2..9  thread (r, h) owns key row r (TMEM lane r) and column half h
+//               (warps 2-5: h = 0, warps 6-9: h = 1).  Phase P (overlaps
+//               dP^T): 64 entries of the P^T row = exp2(S^T * scale*log2e -
+//               LSE2), kept in registers and written to TMEM as BF16, half h
+//               at columns [64h, 64h+32) of its own S^T columns.  Phase dS
+//               (overlaps dV and the next S^T): dS^T = P o (dP^T - D) * scale,
+//               BF16, into shared memory with the 128-byte swizzle both dK and
+//               dQ read.  Phase dQ: half h of query row r of dQ_t, TMEM ->
+//               registers -> the stage buffer in the dq tensor map's box
+//               layout.  At the end: dK, dV rows out of TMEM (FP32).
+// TMEM columns: S^T [0,128) (P^T halves at [0,32) and [64,96)),
+// dP^T / dQ_t [128,256), dV [256,256+d), dK [256+d, 256+2d).
+// Ten warps cap a thread at 168 registers (the register file is split among
+// the four SM sub-partitions, three warps on two of them).
+// All waits are bounded (see sm103_primitives.cuh).
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
 
 namespace fa {
 namespace {
 
+constexpr int kMaxDynSmem = 232448;  // 227 KB opt-in limit per block
+
 template <int D>
 struct BwdCfg {
     static constexpr int BM = 128;  // query rows per Q tile
     static constexpr int BN = 128;  // keys per CTA
     static constexpr int KB = D / 64;
-    static constexpr int BOX_BYTES = 128 * 64 * 2;
-    static constexpr int TILE_BYTES = KB * BOX_BYTES;
-    static constexpr int NSQ = (D == 128) ? 1 : 2;  // Q/dO ring depth
-    static constexpr int DS_BYTES = 2 * BOX_BYTES;  // 128 x 128 bf16
+    static constexpr int BOX_BYTES = 128 * 64 * 2;      // 128 x 64 bf16 = 128 x 32 fp32
+    static constexpr int TILE_BYTES = KB * BOX_BYTES;    // 128 x D bf16
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // [Q | dO] = 128 x D fp32 (dQ)
+    static constexpr int NSQ = 2;                        // stage ring depth
+    static constexpr int DS_BYTES = 2 * BOX_BYTES;       // 128 x 128 bf16
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + TILE_BYTES;
-    static constexpr int OFF_Q = OFF_V + TILE_BYTES;
-    static constexpr int OFF_DO = OFF_Q + NSQ * TILE_BYTES;
-    static constexpr int OFF_DS = OFF_DO + NSQ * TILE_BYTES;
-    static constexpr int OFF_VEC = OFF_DS + DS_BYTES;      // NSQ x (lse2[128], delta[128])
+    static constexpr int OFF_STAGE = OFF_V + TILE_BYTES;
+    static constexpr int OFF_DS = OFF_STAGE + NSQ * STAGE_BYTES;
+    static constexpr int OFF_VEC = OFF_DS + DS_BYTES;  // NSQ x (lse2[128], delta[128])
     static constexpr int OFF_BAR = OFF_VEC + NSQ * 1024;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
+    static constexpr int LAYOUT_BYTES = OFF_BAR + BAR_BYTES;
+    static constexpr int SMEM_BYTES =
+        (LAYOUT_BYTES + 1024 <= kMaxDynSmem) ? LAYOUT_BYTES + 1024 : kMaxDynSmem;
+    static_assert(LAYOUT_BYTES <= kMaxDynSmem, "backward tiles do not fit in shared memory");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 320;
+    static constexpr int COMPUTE_WARPS = 8;
 };
 
 template <int NSQ>
 struct BwdBars {
     static constexpr int KV_FULL = 0;
     static constexpr int Q_FULL = 1;
-    static constexpr int Q_EMPTY = Q_FULL + NSQ;
-    static constexpr int SP_FULL = Q_EMPTY + NSQ;
-    static constexpr int DS_FULL = SP_FULL + 1;
+    static constexpr int S_FULL = Q_FULL + NSQ;
+    static constexpr int DP_FULL = S_FULL + 1;
+    static constexpr int P_FULL = DP_FULL + 1;
+    static constexpr int DS_FULL = P_FULL + 1;
     static constexpr int DQ_FULL = DS_FULL + 1;
     static constexpr int DQ_EMPTY = DQ_FULL + 1;
-    static constexpr int ACC_FULL = DQ_EMPTY + 1;
+    static constexpr int DQ_STAGED = DQ_EMPTY + 1;
+    static constexpr int ACC_FULL = DQ_STAGED + 1;
     static constexpr int DONE = ACC_FULL + 1;
     static constexpr int COUNT = DONE + 1;
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bwd_dkdv_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dq,
                          const float* __restrict__ delta, const float* __restrict__ lse2,
-                         float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
-                         int N, int n_pad, int BH, int n_tiles, float scale, float scale_log2,
+                         float* __restrict__ dk, float* __restrict__ dv, int N, int n_pad,
+                         int BH, int n_tiles, int group, float scale, float scale_log2,
                          unsigned int* status, unsigned long long timeout_ns) {
     using C = BwdCfg<D>;
     using Bar = BwdBars<C::NSQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
+    if (smem + C::LAYOUT_BYTES > smem_raw + C::SMEM_BYTES) {
+        // The dynamic shared memory did not start on a 1024-byte boundary and
+        // the tiles do not fit after aligning: report it and do nothing.
+        if (threadIdx.x == 0) atomicOr(status, kStatusSmemLayout);
+        return;
+    }
     const uint32_t s_base = smem_u32(smem);
     const uint32_t s_k = s_base + C::OFF_K;
     const uint32_t s_v = s_base + C::OFF_V;
-    const uint32_t s_q = s_base + C::OFF_Q;
-    const uint32_t s_do = s_base + C::OFF_DO;
+    const uint32_t s_stage = s_base + C::OFF_STAGE;
     const uint32_t s_ds = s_base + C::OFF_DS;
     const uint32_t s_vec = s_base + C::OFF_VEC;
     const uint32_t s_bar = s_base + C::OFF_BAR;
     auto bar = [&](int slot) -> uint32_t { return s_bar + 8u * static_cast<uint32_t>(slot); };
+    auto q_of = [&](int st) -> uint32_t { return s_stage + st * C::STAGE_BYTES; };
+    auto do_of = [&](int st) -> uint32_t { return s_stage + st * C::STAGE_BYTES + C::TILE_BYTES; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * Bar::COUNT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-    // Key tile 0 sees every Q tile under a causal mask: launch it first.
+    // Key tile 0 sees every Q tile under a causal mask: heavy tiles first,
+    // a few heads at a time so their Q, dO and dq stay in L2.
     const long long lin = blockIdx.x + static_cast<long long>(gridDim.x) *
                                            (blockIdx.y + static_cast<long long>(gridDim.y) *
                                                              blockIdx.z);
-    const int kt = static_cast<int>(lin / BH);
-    const int bh = static_cast<int>(lin % BH);
+    const TileHead th = grouped_order(lin, BH, n_tiles, group, false);
+    const int kt = th.tile;
+    const int bh = th.head;
     const int i0 = CAUSAL ? kt : 0;
     const int n_q = n_tiles - i0;
 
@@ -110,14 +143,14 @@ __global__ void __launch_bounds__(192, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(Bar::KV_FULL), 1);
-        for (int s = 0; s < C::NSQ; ++s) {
-            mbar_init(bar(Bar::Q_FULL + s), 1);
-            mbar_init(bar(Bar::Q_EMPTY + s), 1);
-        }
-        mbar_init(bar(Bar::SP_FULL), 1);
-        mbar_init(bar(Bar::DS_FULL), 4);
+        for (int s = 0; s < C::NSQ; ++s) mbar_init(bar(Bar::Q_FULL + s), 1);
+        mbar_init(bar(Bar::S_FULL), 1);
+        mbar_init(bar(Bar::DP_FULL), 1);
+        mbar_init(bar(Bar::P_FULL), C::COMPUTE_WARPS);
+        mbar_init(bar(Bar::DS_FULL), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::DQ_FULL), 1);
-        mbar_init(bar(Bar::DQ_EMPTY), 4);
+        mbar_init(bar(Bar::DQ_EMPTY), C::COMPUTE_WARPS);
+        mbar_init(bar(Bar::DQ_STAGED), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::ACC_FULL), 1);
         mbar_init(bar(Bar::DONE), 1);
         *abort_flag = 0;
@@ -126,6 +159,7 @@ __global__ void __launch_bounds__(192, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_do);
+        prefetch_tensormap(&tm_dq);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -136,10 +170,25 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const WaitCtx wc{status, timeout_ns, abort_flag};
+    const long long head_row0 = static_cast<long long>(bh) * N;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            auto load_tile = [&](int t) {
+                const int st = t % C::NSQ;
+                const int i = i0 + t;
+                const uint32_t fb = bar(Bar::Q_FULL + st);
+                mbar_arrive_expect_tx(fb, C::STAGE_BYTES + 1024);
+                for (int kb = 0; kb < C::KB; ++kb) {
+                    tma_load_3d(q_of(st) + kb * C::BOX_BYTES, &tm_q, fb, kb * 64, i * C::BM, bh);
+                    tma_load_3d(do_of(st) + kb * C::BOX_BYTES, &tm_do, fb, kb * 64, i * C::BM,
+                                bh);
+                }
+                const long long voff = static_cast<long long>(bh) * n_pad + i * C::BM;
+                bulk_load(s_vec + st * 1024, lse2 + voff, 512, fb);
+                bulk_load(s_vec + st * 1024 + 512, delta + voff, 512, fb);
+            };
             mbar_arrive_expect_tx(bar(Bar::KV_FULL), 2 * C::TILE_BYTES);
             for (int kb = 0; kb < C::KB; ++kb) {
                 tma_load_3d(s_k + kb * C::BOX_BYTES, &tm_k, bar(Bar::KV_FULL), kb * 64,
@@ -148,24 +197,19 @@ __global__ void __launch_bounds__(192, 1)
                             kt * C::BN, bh);
             }
             int issued = 0;
+            for (; issued < n_q && issued < C::NSQ; ++issued) load_tile(issued);
             for (int t = 0; t < n_q; ++t) {
                 const int st = t % C::NSQ;
-                const int use = t / C::NSQ;
-                if (use > 0 && !mbar_wait(bar(Bar::Q_EMPTY + st), (use - 1) & 1, wc)) break;
-                const int i = i0 + t;
-                const uint32_t fb = bar(Bar::Q_FULL + st);
-                mbar_arrive_expect_tx(fb, 2 * C::TILE_BYTES + 1024);
-                for (int kb = 0; kb < C::KB; ++kb) {
-                    tma_load_3d(s_q + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_q, fb,
-                                kb * 64, i * C::BM, bh);
-                    tma_load_3d(s_do + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_do, fb,
-                                kb * 64, i * C::BM, bh);
-                }
-                const long long voff = static_cast<long long>(bh) * n_pad + i * C::BM;
-                bulk_load(s_vec + st * 1024, lse2 + voff, 512, fb);
-                bulk_load(s_vec + st * 1024 + 512, delta + voff, 512, fb);
-                issued = t + 1;
+                if (!mbar_wait(bar(Bar::DQ_STAGED), t & 1, wc)) break;
+                // dQ_t sits in stage st in the dq map's box layout: add it into dq.
+                for (int b = 0; b < D / 32; ++b)
+                    tma_reduce_add_3d(&tm_dq, q_of(st) + b * C::BOX_BYTES, b * 32,
+                                      (i0 + t) * C::BM, bh);
+                bulk_commit();
+                bulk_wait_read_all();
+                if (issued < n_q) load_tile(issued++);
             }
+            bulk_wait_all();
             mbar_wait_drain(bar(Bar::KV_FULL), 0, timeout_ns);
             for (int t = (issued > C::NSQ ? issued - C::NSQ : 0); t < issued; ++t)
                 mbar_wait_drain(bar(Bar::Q_FULL + t % C::NSQ), (t / C::NSQ) & 1, timeout_ns);
@@ -176,151 +220,185 @@ __global__ void __launch_bounds__(192, 1)
             constexpr uint32_t id_sp = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
             constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);    // dV, dK: B MN-major
             constexpr uint32_t id_q = idesc_bf16(128, D, 1, 1);     // dQ: A and B MN-major
-            bool ok = mbar_wait(bar(Bar::KV_FULL), 0, wc);
-            for (int t = 0; t < n_q && ok; ++t) {
+            auto issue_s = [&](int t) -> bool {  // S^T_t = K Q_t^T
                 const int st = t % C::NSQ;
-                const uint32_t q_tile = s_q + st * C::TILE_BYTES;
-                const uint32_t do_tile = s_do + st * C::TILE_BYTES;
-                ok = mbar_wait(bar(Bar::Q_FULL + st), (t / C::NSQ) & 1, wc);
-                if (ok && t > 0) ok = mbar_wait(bar(Bar::DQ_EMPTY), (t - 1) & 1, wc);
-                if (!ok) break;
+                if (!mbar_wait(bar(Bar::Q_FULL + st), (t / C::NSQ) & 1, wc)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
                     mma_ss(tmem + C::COL_S, smem_desc_sw128(s_k + koff, 16, 1024),
-                           smem_desc_sw128(q_tile + koff, 16, 1024), id_sp, kk > 0);
+                           smem_desc_sw128(q_of(st) + koff, 16, 1024), id_sp, kk > 0);
+                }
+                tc_commit(bar(Bar::S_FULL));
+                return true;
+            };
+            bool ok = mbar_wait(bar(Bar::KV_FULL), 0, wc) && issue_s(0);
+            for (int t = 0; t < n_q && ok; ++t) {
+                const int st = t % C::NSQ;
+                if (t > 0) {  // dQ_{t-1} must be out of the DP columns
+                    ok = mbar_wait(bar(Bar::DQ_EMPTY), (t - 1) & 1, wc);
+                    if (!ok) break;
+                    tc_fence_after();
                 }
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO_t^T
                     const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
                     mma_ss(tmem + C::COL_DP, smem_desc_sw128(s_v + koff, 16, 1024),
-                           smem_desc_sw128(do_tile + koff, 16, 1024), id_sp, kk > 0);
+                           smem_desc_sw128(do_of(st) + koff, 16, 1024), id_sp, kk > 0);
                 }
-                tc_commit(bar(Bar::SP_FULL));
+                tc_commit(bar(Bar::DP_FULL));
+                const uint32_t acc = (t > 0) ? 1u : 0u;
+                ok = mbar_wait(bar(Bar::P_FULL), t & 1, wc);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk) {  // dV += P^T dO_t
+                    // P^T halves: queries 0-63 at columns [0,32), 64-127 at [64,96).
+                    const uint32_t pcol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                    mma_ts(tmem + C::COL_DV, tmem + C::COL_S + pcol,
+                           smem_desc_sw128(do_of(st) + kk * 2048, C::BOX_BYTES, 1024), id_kv,
+                           acc | (kk > 0));
+                }
+                if (t + 1 < n_q) {
+                    ok = issue_s(t + 1);
+                    if (!ok) break;
+                }
                 ok = mbar_wait(bar(Bar::DS_FULL), t & 1, wc);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t acc = (t > 0) ? 1u : 0u;
 #pragma unroll
-                for (int kk = 0; kk < C::BM / 16; ++kk)  // dV += P^T dO_i
-                    mma_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8,
-                           smem_desc_sw128(do_tile + kk * 2048, C::BOX_BYTES, 1024), id_kv,
-                           acc | (kk > 0));
-#pragma unroll
-                for (int kk = 0; kk < C::BM / 16; ++kk)  // dK += dS^T Q_i
+                for (int kk = 0; kk < C::BM / 16; ++kk)  // dK += dS^T Q_t
                     mma_ss(tmem + C::COL_DK,
                            smem_desc_sw128(s_ds + (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32, 16,
                                            1024),
-                           smem_desc_sw128(q_tile + kk * 2048, C::BOX_BYTES, 1024), id_kv,
+                           smem_desc_sw128(q_of(st) + kk * 2048, C::BOX_BYTES, 1024), id_kv,
                            acc | (kk > 0));
 #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)  // dQ_i = dS K
+                for (int kk = 0; kk < C::BN / 16; ++kk)  // dQ_t = dS K
                     mma_ss(tmem + C::COL_DP,
                            smem_desc_sw128(s_ds + kk * 2048, C::BOX_BYTES, 1024),
                            smem_desc_sw128(s_k + kk * 2048, C::BOX_BYTES, 1024), id_q, kk > 0);
-                tc_commit(bar(Bar::Q_EMPTY + st));
                 tc_commit(bar(Bar::DQ_FULL));
             }
             if (ok) tc_commit(bar(Bar::ACC_FULL));
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ compute
+        // ------------------------------------------------------------ P / dS / dQ
         const int wq = warp & 3;
-        const int r = wq * 32 + lane;            // key row (then query row for dQ)
-        const int kglob = kt * C::BN + r;        // key index inside the head
+        const int h = (warp - 2) >> 2;       // column half
+        const int r = wq * 32 + lane;        // key row (query row in phase dQ)
+        const int kglob = kt * C::BN + r;    // key index inside the head
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const float* vec_base = reinterpret_cast<const float*>(smem + C::OFF_VEC);
-        uint8_t* ds_rows = smem + C::OFF_DS;
-        const long long head_row0 = static_cast<long long>(bh) * N;
+        uint8_t* ds_box = smem + C::OFF_DS + h * C::BOX_BYTES;
+        const bool key_pad = kglob >= N;
         bool ok = true;
         for (int t = 0; t < n_q; ++t) {
             const int st = t % C::NSQ;
             const int i = i0 + t;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::SP_FULL), t & 1, wc) &&
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_FULL), t & 1, wc) &&
                                              mbar_wait(bar(Bar::Q_FULL + st),
                                                        (t / C::NSQ) & 1, wc));
             if (!ok) break;
             tc_fence_after();
-            const float* l2v = vec_base + st * 256;
-            const float* dlt = l2v + 128;
-            const bool diag = CAUSAL && i == kt;
-            const bool key_pad = kglob >= N;
+            const float* l2v = vec_base + st * 256 + 64 * h;
+            const float* dlt = vec_base + st * 256 + 128 + 64 * h;
+            // Phase P: entries [64h, 64h+64) of this key's row of P^T.
+            float p[64];
+            {
+                uint32_t sr[64];
+                tmem_ld64(t_lane + C::COL_S + 64 * h, sr);
+                const int q0 = i * C::BM + 64 * h;  // query index of entry 0
+                if (key_pad || (CAUSAL && i == kt)) {
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(t_lane + C::COL_S + ch * 32, sr);
-                tmem_ld32(t_lane + C::COL_DP + ch * 32, dr);
-                uint32_t pk[16];
-                uint32_t dk2[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pe[2], de[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = ch * 32 + 2 * e + h;  // query column in the tile
-                        float p = ex2_approx(
-                            fmaf(__uint_as_float(sr[2 * e + h]), scale_log2, -l2v[c]));
-                        if (key_pad || (diag && i * C::BM + c < kglob)) p = 0.f;
-                        pe[h] = p;
-                        de[h] = p * (__uint_as_float(dr[2 * e + h]) - dlt[c]) * scale;
+                    for (int c = 0; c < 64; ++c) {
+                        const float x =
+                            ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, -l2v[c]));
+                        p[c] = (key_pad || q0 + c < kglob) ? 0.f : x;
                     }
-                    pk[e] = pack_bf16x2(pe[0], pe[1]);
-                    dk2[e] = pack_bf16x2(de[0], de[1]);
-                }
-                tmem_st16(t_lane + C::COL_S + ch * 16, pk);
-                // dS^T row r, queries ch*32 .. ch*32+31: four 16-byte chunks.
-                const int box = ch >> 1;
+                } else {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int chunk = ((ch & 1) * 4 + u) ^ (r & 7);
-                    *reinterpret_cast<uint4*>(ds_rows + box * C::BOX_BYTES + r * 128 +
-                                              chunk * 16) =
-                        make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+                    for (int c = 0; c < 64; ++c)
+                        p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, -l2v[c]));
                 }
             }
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+                tmem_st32(t_lane + C::COL_S + 64 * h, pk);
+            }
             tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Bar::P_FULL));
+
+            // Phase dS: dS^T = P o (dP^T - D) * scale into smem box h, row r.
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DP_FULL), t & 1, wc));
+            if (!ok) break;
+            tc_fence_after();
+            {
+                uint32_t dr[64];
+                tmem_ld64(t_lane + C::COL_DP + 64 * h, dr);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 8 * u + 2 * e;
+                        w[e] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - dlt[c]) * scale,
+                                           p[c + 1] * (__uint_as_float(dr[c + 1]) - dlt[c + 1]) *
+                                               scale);
+                    }
+                    *reinterpret_cast<uint4*>(ds_box + r * 128 + ((u ^ (r & 7)) * 16)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(Bar::DS_FULL));
 
-            // dQ_i tile: lane r now owns query row r of the tile.
+            // Phase dQ: half h of query row r of dQ_t into stage st, box layout
+            // of the dq tensor map (128 rows x 32 fp32, 128-byte swizzle).
             ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DQ_FULL), t & 1, wc));
             if (!ok) break;
             tc_fence_after();
-            const int qglob = i * C::BM + r;
-            float4* dq_row = reinterpret_cast<float4*>(dq + (head_row0 + qglob) * D);
+            uint8_t* stage = smem + C::OFF_STAGE + st * C::STAGE_BYTES;
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
+            for (int bb = 0; bb < D / 64; ++bb) {
                 uint32_t qr[32];
-                tmem_ld32(t_lane + C::COL_DP + ch * 32, qr);
-                if (qglob < N) {
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        atomicAdd(dq_row + ch * 8 + u,
-                                  make_float4(__uint_as_float(qr[4 * u]),
-                                              __uint_as_float(qr[4 * u + 1]),
-                                              __uint_as_float(qr[4 * u + 2]),
-                                              __uint_as_float(qr[4 * u + 3])));
+                tmem_ld32(t_lane + C::COL_DP + (D / 2) * h + 32 * bb, qr);
+                if (bb == D / 64 - 1) {
+                    // Every dQ column of this lane is in registers: free the DP
+                    // columns for the next dP^T.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(Bar::DQ_EMPTY));
                 }
+                uint8_t* box = stage + ((D / 64) * h + bb) * C::BOX_BYTES + r * 128;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<uint4*>(box + ((u ^ (r & 7)) * 16)) =
+                        make_uint4(qr[4 * u], qr[4 * u + 1], qr[4 * u + 2], qr[4 * u + 3]);
             }
-            tc_fence_before();
+            fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Bar::DQ_EMPTY));
+            if (lane == 0) mbar_arrive(bar(Bar::DQ_STAGED));
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::ACC_FULL), 0, wc));
         if (ok) {
             tc_fence_after();
-            float4* dv_row = reinterpret_cast<float4*>(dv + (head_row0 + kglob) * D);
-            float4* dk_row = reinterpret_cast<float4*>(dk + (head_row0 + kglob) * D);
+            float4* dv_row = reinterpret_cast<float4*>(dv + (head_row0 + kglob) * D + (D / 2) * h);
+            float4* dk_row = reinterpret_cast<float4*>(dk + (head_row0 + kglob) * D + (D / 2) * h);
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
+            for (int ch = 0; ch < D / 64; ++ch) {
                 uint32_t a[32], b[32];
-                tmem_ld32(t_lane + C::COL_DV + ch * 32, a);
-                tmem_ld32(t_lane + C::COL_DK + ch * 32, b);
-                if (kglob < N) {
+                tmem_ld32(t_lane + C::COL_DV + (D / 2) * h + ch * 32, a);
+                tmem_ld32(t_lane + C::COL_DK + (D / 2) * h + ch * 32, b);
+                if (!key_pad) {
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         dv_row[ch * 8 + u] =
@@ -358,10 +436,13 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_tiles = (a.N + C::BN - 1) / C::BN;
+    // Enough heads per group that a group fills about one wave of CTAs.
+    int group = 128 / n_tiles;
+    if (group < 1) group = 1;
     dim3 grid(n_tiles, a.H, a.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, a.delta, a.lse2, a.dq, a.dk, a.dv, a.N, a.n_pad,
-        a.B * a.H, n_tiles, a.scale, a.scale_log2, a.status, a.timeout_ns);
+        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, a.delta, a.lse2, a.dk, a.dv, a.N,
+        a.n_pad, a.B * a.H, n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
     return cudaGetLastError();
 }
 

@@ -78,6 +78,24 @@ int make_map_bf16(CUtensorMap* map, const void* ptr, int d, int N, long long BH)
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// [B*H, N, d] fp32 viewed as (d, N, B*H); 128-row x 32-column boxes (128
+// bytes wide, 128-byte swizzle): the dQ bulk-reduction target.
+int make_map_f32(CUtensorMap* map, const void* ptr, int d, int N, long long BH) {
+    EncodeFn enc;
+    if (int rc = get_encode(&enc)) return rc;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 4};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(int B, int H, int N, int d, float scale) {
@@ -132,7 +150,8 @@ int fa_device_status(int clear) {
         if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(zero)) != cudaSuccess)
             return FA_ERR_CUDA;
     }
-    return word ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+    if (word & 1u) return FA_ERR_DEVICE_TIMEOUT;
+    return word ? FA_ERR_CUDA : FA_OK;  // bit 1: a kernel found its shared memory misplaced
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
@@ -176,12 +195,13 @@ int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
     unsigned int* status;
     if (int rc = status_ptr(&status)) return rc;
     const long long BH = static_cast<long long>(B) * H;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
-    fa::BwdArgs a{&tq, &tk, &tv, &tdo, delta_ws, lse2_ws, dq, dk, dv, B, H, N, d,
+    if (int rc = make_map_f32(&tdq, dq, d, N, BH)) return rc;
+    fa::BwdArgs a{&tq, &tk, &tv, &tdo, &tdq, delta_ws, lse2_ws, dk, dv, B, H, N, d,
                   static_cast<int>(n_pad_of(N)), causal ? 1 : 0, scale,
                   scale * 1.4426950408889634f, status, g_timeout_ns.load()};
     return launch_rc(fa::launch_bwd_dkdv_bf16(a, static_cast<cudaStream_t>(stream)));

@@ -40,15 +40,17 @@ struct BwdPreArgs {
 
 cudaError_t launch_bwd_pre_bf16(const BwdPreArgs& a, cudaStream_t stream);
 
-// Backward dK/dV + dQ (BF16).  Tensor maps as for the forward.
+// Backward dK/dV + dQ (BF16).  Tensor maps for Q, K, V, dO as for the
+// forward; tm_dq views dq as (d, N, B*H) fp32 in 128-row x 32-column boxes
+// (128-byte swizzle), the target of the dQ bulk reductions.
 struct BwdArgs {
     const CUtensorMap* tm_q;
     const CUtensorMap* tm_k;
     const CUtensorMap* tm_v;
     const CUtensorMap* tm_do;
+    const CUtensorMap* tm_dq;
     const float* delta;
     const float* lse2;
-    float* dq;
     float* dk;
     float* dv;
     int B, H, N, d, n_pad;

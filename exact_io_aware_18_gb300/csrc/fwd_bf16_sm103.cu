@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(192, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, float* __restrict__ lse, int N,
-                    int BH, int n_tiles, float scale_log2, unsigned int* status,
+                    int BH, int n_tiles, int group, float scale_log2, unsigned int* status,
                     unsigned long long timeout_ns) {
     using C = FwdCfg<D>;
     using Bar = FwdBars<C::NS>;
@@ -89,12 +89,14 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * Bar::COUNT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-    // Heavy tiles first: with a causal mask the last Q tile sees the most keys.
+    // Heavy tiles first (with a causal mask the last Q tile sees the most
+    // keys), a few heads at a time so that their K/V tiles stay in L2.
     const long long lin = blockIdx.x + static_cast<long long>(gridDim.x) *
                                            (blockIdx.y + static_cast<long long>(gridDim.y) *
                                                              blockIdx.z);
-    const int qt = n_tiles - 1 - static_cast<int>(lin / BH);
-    const int bh = static_cast<int>(lin % BH);
+    const TileHead th = grouped_order(lin, BH, n_tiles, group, true);
+    const int qt = th.tile;
+    const int bh = th.head;
     const int n_kv = CAUSAL ? qt + 1 : n_tiles;
 
     const int warp = threadIdx.x >> 5;
@@ -355,10 +357,13 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_tiles = (a.N + C::BM - 1) / C::BM;
+    // Enough heads per group that a group fills about one wave of CTAs.
+    int group = 128 / n_tiles;
+    if (group < 1) group = 1;
     dim3 grid(n_tiles, a.H, a.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse,
-                                                       a.N, a.B * a.H, n_tiles, a.scale_log2,
-                                                       a.status, a.timeout_ns);
+                                                       a.N, a.B * a.H, n_tiles, group,
+                                                       a.scale_log2, a.status, a.timeout_ns);
     return cudaGetLastError();
 }
 

@@ -42,7 +42,7 @@ WORKLOAD = "training step fwd+bwd, bf16, B=8 H=16 N=2048 d=128, causal, scale=1/
 # DRAM traffic of one dK/dV launch at this workload, from
 # profiles/kernels_training_step_b8_h16_n2048_d128_causal.md; valid only for the kernel
 # source it was measured on (sha256 of csrc/bwd_bf16_sm103.cu).
-DKDV_TRAFFIC = {"bytes": 3018670000, "src_sha256": "8400ed945337925c60d3056fdb8c14b9996aa47240331a5d021ea1bf9151c124"}
+DKDV_TRAFFIC = {"bytes": 756726016, "src_sha256": "2a7d8e24bf5fb62fad1faf053c396001ddcf6420aa6721c865badcd7c31f34e3"}
 DKDV_SRC = os.path.join(ROOT, "exact_io_aware_18_gb300", "csrc", "bwd_bf16_sm103.cu")
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}

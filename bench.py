@@ -2,8 +2,8 @@
 
 One step = the whole hot path over one batch of the training-step workload
 (bf16, B=8 H=16 N=2048 d=128, causal, scale 1/sqrt(d), seeded N(0,1) Q, K, V,
-dO): the forward (O, LSE), then the backward preprocess (D, dq = 0) and the
-dK/dV kernel with the dQ accumulation.  The metric counts 4 B H N^2 d FLOPs
+dO): the forward (O, LSE), then the backward preprocess (D, base-2 LSE), the
+dK/dV kernel and the dQ kernel.  The metric counts 4 B H N^2 d FLOPs
 for the forward and 2.5x that for the backward, halved for the causal mask.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -39,11 +39,14 @@ METRIC = ("attention fwd/bwd TFLOP/s (4BHN²d, causal halved) and % of GB300 BF1
 B, H, N, D, CAUSAL, SEED = 8, 16, 2048, 128, True, 4
 WORKLOAD = "training step fwd+bwd, bf16, B=8 H=16 N=2048 d=128, causal, scale=1/sqrt(d), seed 4"
 
-# DRAM traffic of one dK/dV launch at this workload, from
-# profiles/kernels_training_step_b8_h16_n2048_d128_causal.md; valid only for the kernel
-# source it was measured on (sha256 of csrc/bwd_bf16_sm103.cu).
-DKDV_TRAFFIC = {"bytes": 756726016, "src_sha256": "2a7d8e24bf5fb62fad1faf053c396001ddcf6420aa6721c865badcd7c31f34e3"}
-DKDV_SRC = os.path.join(ROOT, "exact_io_aware_18_gb300", "csrc", "bwd_bf16_sm103.cu")
+# DRAM traffic of one launch of a kernel at this workload, from the ncu
+# summaries under profiles/; valid only for the kernel source it was measured
+# on (sha256 of its .cu file), else the roofline reports traffic as null.
+CSRC = os.path.join(ROOT, "exact_io_aware_18_gb300", "csrc")
+KERNEL_SRC = {"fwd_bf16": os.path.join(CSRC, "fwd_bf16_sm103.cu"),
+              "bwd_dkdv_bf16": os.path.join(CSRC, "bwd_bf16_sm103.cu"),
+              "bwd_dq_bf16": os.path.join(CSRC, "bwd_dq_sm103.cu")}
+KERNEL_TRAFFIC = {}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -196,12 +199,15 @@ def run_gpu(args):
         fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream)
         if ev is not None:
             ev[1].record(stream)
-        fa.fa_bwd_preprocess(o, do, lse, delta, lse2, dq, stream)
+        fa.fa_bwd_preprocess(o, do, lse, delta, lse2, stream)
         if ev is not None:
             ev[2].record(stream)
-        fa.fa_bwd_dkdv(q, k, v, do, delta, lse2, dq, dk, dv, CAUSAL, scale, stream)
+        fa.fa_bwd_dkdv(q, k, v, do, delta, lse2, dk, dv, CAUSAL, scale, stream)
         if ev is not None:
             ev[3].record(stream)
+        fa.fa_bwd_dq(q, k, v, do, delta, lse2, dq, CAUSAL, scale, stream)
+        if ev is not None:
+            ev[4].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -220,7 +226,7 @@ def run_gpu(args):
     sampler.start()
     time.sleep(0.3)
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -246,6 +252,7 @@ def run_gpu(args):
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
     pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
     dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in events)
+    dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in events)
 
     # End to end through the public calls: pinned host inputs in, outputs back.
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
@@ -288,14 +295,23 @@ def run_gpu(args):
     value = world * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
     peaks, peak_kind = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    achieved = f_bwd / (dkdv_ms * 1e-3) / 1e12
+    # Each kernel's own GEMM FLOPs per launch: the forward does 2 GEMMs per
+    # (Q tile, key tile) pair, dK/dV 4 (S^T, dP^T, dV, dK), dQ 3 (S, dP, dQ;
+    # S and dP recomputed).  The step metric counts 2.5x the forward for the
+    # whole backward, as the workload's metric does.
+    kern_flops = {"fwd_bf16": f_fwd, "bwd_dkdv_bf16": 2.0 * f_fwd, "bwd_dq_bf16": 1.5 * f_fwd}
+    kern_ms = {"fwd_bf16": fwd_ms, "bwd_dkdv_bf16": dkdv_ms, "bwd_dq_bf16": dq_ms}
+    dominant = max(kern_ms, key=kern_ms.get)
+    achieved = kern_flops[dominant] / (kern_ms[dominant] * 1e-3) / 1e12
     traffic = None
     try:
-        with open(DKDV_SRC, "rb") as fsrc:
+        src = KERNEL_SRC[dominant]
+        with open(src, "rb") as fsrc:
             sha = hashlib.sha256(fsrc.read()).hexdigest()
-        if DKDV_TRAFFIC["bytes"] and DKDV_TRAFFIC["src_sha256"] == sha:
-            traffic = DKDV_TRAFFIC["bytes"]
-    except OSError:
+        rec = KERNEL_TRAFFIC.get(dominant)
+        if rec and rec["bytes"] and rec["src_sha256"] == sha:
+            traffic = rec["bytes"]
+    except (OSError, KeyError):
         pass
     clocks = sampler.summary(t_wall0, t_wall1)
 
@@ -305,8 +321,7 @@ def run_gpu(args):
     cpu_s, cpu_flops = oracle_step_sample(x, n_heads)
 
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    pre_bytes = (2 * B * H * N * D * 2 + B * H * N * 4 + 2 * B * H * n_pad * 4
-                 + B * H * N * D * 4)
+    pre_bytes = 2 * B * H * N * D * 2 + B * H * N * 4 + 2 * B * H * n_pad * 4
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -322,7 +337,7 @@ def run_gpu(args):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "causal": CAUSAL,
                    "l2": "inputs larger than L2: Q, K, V, dO are 4 x 64 MiB per step"},
-        "roofline": {"bound": "tensor", "kernel": "bwd_dkdv_bf16", "achieved": round(achieved, 2),
+        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": f"bf16_tflops_sustained ({peak_kind})",
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic},
         "cpu_baseline": {"value": round(cpu_flops / cpu_s / 1e12, 6), "unit": "TFLOP/s",
@@ -332,7 +347,7 @@ def run_gpu(args):
         "e2e": {"value": round(world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "kernels": {
             "fwd": {"ms": round(fwd_ms, 4), "tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
@@ -340,8 +355,11 @@ def run_gpu(args):
             "bwd_preprocess": {"ms": round(pre_ms, 4),
                                "gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
                                "frac_of_hbm": round(pre_bytes / (pre_ms * 1e-3) / 1e9 / hbm, 4)},
-            "bwd_dkdv": {"ms": round(dkdv_ms, 4), "tflops": round(achieved, 2)},
-            "bwd_total_tflops": round(f_bwd / ((pre_ms + dkdv_ms) * 1e-3) / 1e12, 2),
+            "bwd_dkdv": {"ms": round(dkdv_ms, 4),
+                         "tflops": round(kern_flops["bwd_dkdv_bf16"] / (dkdv_ms * 1e-3) / 1e12, 2)},
+            "bwd_dq": {"ms": round(dq_ms, 4),
+                       "tflops": round(kern_flops["bwd_dq_bf16"] / (dq_ms * 1e-3) / 1e12, 2)},
+            "bwd_total_tflops": round(f_bwd / ((pre_ms + dkdv_ms + dq_ms) * 1e-3) / 1e12, 2),
         },
     }
     print(json.dumps(out), flush=True)

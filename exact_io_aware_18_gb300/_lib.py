@@ -35,8 +35,9 @@ _SIGNATURES = {
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_bwd_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "fa_bwd": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _sz, _vp], _i),
-    "fa_bwd_preprocess": ([_vp] * 6 + [_i, _i, _i, _i, _vp], _i),
-    "fa_bwd_dkdv": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_bwd_preprocess": ([_vp] * 5 + [_i, _i, _i, _i, _vp], _i),
+    "fa_bwd_dkdv": ([_vp] * 8 + [_i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_bwd_dq": ([_vp] * 7 + [_i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_fwd_f32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_bwd_f32": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _sz, _vp], _i),
     "fa_error_string": ([_i], ctypes.c_char_p),
@@ -149,8 +150,8 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, workspac
                          _ptr(workspace), ws_bytes, _stream(stream)), "fa_bwd")
 
 
-def fa_bwd_preprocess(o, do, lse, delta_ws, lse2_ws, dq, stream=None) -> None:
-    """D = rowsum(dO o O) and LSE*log2(e) into padded [B*H, roundup(N,128)] vectors; dq = 0."""
+def fa_bwd_preprocess(o, do, lse, delta_ws, lse2_ws, stream=None) -> None:
+    """D = rowsum(dO o O) and LSE*log2(e) into padded [B*H, roundup(N,128)] vectors."""
     B, H, N, d = _bhnd(o)
     n_pad = (N + 127) // 128 * 128
     _expect(o, "o", torch.bfloat16, (B, H, N, d))
@@ -158,25 +159,39 @@ def fa_bwd_preprocess(o, do, lse, delta_ws, lse2_ws, dq, stream=None) -> None:
     _expect(lse, "lse", torch.float32, (B, H, N))
     _expect(delta_ws, "delta_ws", torch.float32, (B * H, n_pad))
     _expect(lse2_ws, "lse2_ws", torch.float32, (B * H, n_pad))
-    _expect(dq, "dq", torch.float32, (B, H, N, d))
     _check(load().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), _ptr(delta_ws), _ptr(lse2_ws),
-                                    _ptr(dq), B, H, N, d, _stream(stream)), "fa_bwd_preprocess")
+                                    B, H, N, d, _stream(stream)), "fa_bwd_preprocess")
 
 
-def fa_bwd_dkdv(q, k, v, do, delta_ws, lse2_ws, dq, dk, dv, causal: bool, scale: float,
-                stream=None) -> None:
-    """dK, dV and the dQ accumulation, after fa_bwd_preprocess."""
+def _bwd_step_inputs(q, k, v, do, delta_ws, lse2_ws):
     B, H, N, d = _bhnd(q)
     n_pad = (N + 127) // 128 * 128
     for name, t in (("q", q), ("k", k), ("v", v), ("do", do)):
         _expect(t, name, torch.bfloat16, (B, H, N, d))
     _expect(delta_ws, "delta_ws", torch.float32, (B * H, n_pad))
     _expect(lse2_ws, "lse2_ws", torch.float32, (B * H, n_pad))
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+    return B, H, N, d
+
+
+def fa_bwd_dkdv(q, k, v, do, delta_ws, lse2_ws, dk, dv, causal: bool, scale: float,
+                stream=None) -> None:
+    """dK and dV, after fa_bwd_preprocess."""
+    B, H, N, d = _bwd_step_inputs(q, k, v, do, delta_ws, lse2_ws)
+    for name, t in (("dk", dk), ("dv", dv)):
         _expect(t, name, torch.float32, (B, H, N, d))
     _check(load().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(delta_ws), _ptr(lse2_ws),
-                              _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)),
-                              float(scale), _stream(stream)), "fa_bwd_dkdv")
+                              _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale),
+                              _stream(stream)), "fa_bwd_dkdv")
+
+
+def fa_bwd_dq(q, k, v, do, delta_ws, lse2_ws, dq, causal: bool, scale: float,
+              stream=None) -> None:
+    """dQ, after fa_bwd_preprocess."""
+    B, H, N, d = _bwd_step_inputs(q, k, v, do, delta_ws, lse2_ws)
+    _expect(dq, "dq", torch.float32, (B, H, N, d))
+    _check(load().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(delta_ws), _ptr(lse2_ws),
+                            _ptr(dq), B, H, N, d, int(bool(causal)), float(scale),
+                            _stream(stream)), "fa_bwd_dq")
 
 
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float,

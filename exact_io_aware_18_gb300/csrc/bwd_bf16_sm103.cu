@@ -1,47 +1,47 @@
-// bwd_bf16_sm103.cu - attention backward, dK/dV kernel with the dQ reduction,
-// BF16 in / FP32 accumulate, tcgen05 + TMEM + TMA on sm_103a.
+// bwd_bf16_sm103.cu - attention backward, dK/dV kernel, BF16 in / FP32
+// accumulate, tcgen05 + TMEM + TMA on sm_103a.
 //
 // Method.  The gradient of O = softmax(scale Q K^T) V with the probabilities
 // recomputed from the saved LSE instead of read back ("Flash Attention:
 // Revolutionizing Transformer Efficiency", section "The Flash Attention
 // algorithm", idea 2, recomputation).  Per (b, h), with D_i = dO_i . O_i:
 //   P   = exp(scale S - LSE)      dV = P^T dO        dP = dO V^T
-//   dS  = P o (dP - D)            dQ = scale dS K    dK = scale dS^T Q
+//   dS  = P o (dP - D)            dK = scale dS^T Q  (dQ: bwd_dq_sm103.cu)
 // One CTA owns one 128-key tile j of one (b, h), keeps K_j and V_j in shared
 // memory and dK_j, dV_j in TMEM, and loops over the 128-row Q tiles i that
 // see those keys (i >= j when causal); the parallelism over key tiles of one
 // head is the sequence parallelism of "FlashAttention-2" (technical
-// architecture, improvement 2).  Each dQ_i tile is computed on the tensor
-// core and added into the FP32 dq buffer by a TMA bulk reduction.
+// architecture, improvement 2).  dQ is left to a second kernel that loops
+// over key tiles per Q tile, so nothing here is reduced across CTAs.
 //
-// Roles (320 threads, one CTA per SM):
+// Roles (352 threads, one CTA per SM):
 //   warp 0      TMA producer: K_j, V_j once; per Q tile, into a two-deep ring
 //               of [Q_i | dO_i] stages plus the 128-entry LSE2 / D vectors.
-//               When the compute warps have staged dQ_i (FP32) in that stage
-//               buffer, it issues the bulk reduce-add into dq, waits until the
-//               reduction has read the buffer, and reloads it with Q_{i+2}.
-//   warp 1      MMA issuer.  Tensor-pipe order, per tile t:
-//                 dP^T_t = V dO_t^T        (after dQ_{t-1} left the DP columns)
-//                 dV    += P^T_t dO_t      A = P^T in TMEM (after P_FULL)
-//                 S^T_t+1 = K Q_t+1^T      overwrites P^T_t after dV read it
-//                 dK    += dS^T_t Q_t      A = dS^T in smem (after DS_FULL)
-//                 dQ_t   = dS_t K          A = dS (M-major) -> DP columns
-//               so S^T of the next tile runs while the dS math of this one does.
+//   warps 1, 10 two MMA issuers (one thread each).  A single thread issues a
+//               128 x 128 x 16 tcgen05.mma about as fast as the tensor pipe
+//               runs it, so every barrier check in between would leave the
+//               pipe idle; with two issuers one keeps the pipe fed while the
+//               other waits.  Each issuer overwrites only TMEM it alone reads,
+//               after those reads in its own issue order:
+//                 issuer A: dV += P^T_t dO_t (A = P^T in TMEM, after P_FULL),
+//                           then S^T_t+1 = K Q_t+1^T over P^T_t;
+//                 issuer B: dK += dS^T_t Q_t (A = dS^T in TMEM, after DS_FULL),
+//                           then dP^T_t+1 = V dO_t+1^T over dS^T_t.
+//               So S^T and dP^T of the next tile run while the P and dS math
+//               of this one does.  A stage is free once both issuers commit.
 //   warps 2..9  thread (r, h) owns key row r (TMEM lane r) and column half h
-//               (warps 2-5: h = 0, warps 6-9: h = 1).  Phase P (overlaps
-//               dP^T): 64 entries of the P^T row = exp2(S^T * scale*log2e -
-//               LSE2), kept in registers and written to TMEM as BF16, half h
-//               at columns [64h, 64h+32) of its own S^T columns.  Phase dS
-//               (overlaps dV and the next S^T): dS^T = P o (dP^T - D) * scale,
-//               BF16, into shared memory with the 128-byte swizzle both dK and
-//               dQ read.  Phase dQ: half h of query row r of dQ_t, TMEM ->
-//               registers -> the stage buffer in the dq tensor map's box
-//               layout.  At the end: dK, dV rows out of TMEM (FP32).
+//               (warps 2-5: h = 0, warps 6-9: h = 1).  Phase P: 64 entries of
+//               the P^T row = exp2(S^T * scale*log2e - LSE2), kept in
+//               registers and written back as BF16 into the first 32 of its
+//               own 64 S^T columns.  Phase dS: dS^T = P o (dP^T - D), BF16,
+//               likewise into its own dP^T columns (scale is applied to dK
+//               once, when it leaves TMEM).  At the end: dK, dV rows out of
+//               TMEM to global memory (FP32).
 // TMEM columns: S^T [0,128) (P^T halves at [0,32) and [64,96)),
-// dP^T / dQ_t [128,256), dV [256,256+d), dK [256+d, 256+2d).
-// Ten warps cap a thread at 168 registers (the register file is split among
-// the four SM sub-partitions, three warps on two of them).
-// All waits are bounded (see sm103_primitives.cuh).
+// dP^T [128,256) (dS^T halves at [128,160) and [192,224)), dV [256,256+d),
+// dK [256+d, 256+2d).  Eleven warps cap a thread at 168 registers (the
+// register file is split among the four SM sub-partitions, three warps on
+// three of them).  All waits are bounded (see sm103_primitives.cuh).
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
 
@@ -55,16 +55,14 @@ struct BwdCfg {
     static constexpr int BM = 128;  // query rows per Q tile
     static constexpr int BN = 128;  // keys per CTA
     static constexpr int KB = D / 64;
-    static constexpr int BOX_BYTES = 128 * 64 * 2;      // 128 x 64 bf16 = 128 x 32 fp32
+    static constexpr int BOX_BYTES = 128 * 64 * 2;      // 128 x 64 bf16
     static constexpr int TILE_BYTES = KB * BOX_BYTES;    // 128 x D bf16
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // [Q | dO] = 128 x D fp32 (dQ)
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // [Q | dO]
     static constexpr int NSQ = 2;                        // stage ring depth
-    static constexpr int DS_BYTES = 2 * BOX_BYTES;       // 128 x 128 bf16
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + TILE_BYTES;
     static constexpr int OFF_STAGE = OFF_V + TILE_BYTES;
-    static constexpr int OFF_DS = OFF_STAGE + NSQ * STAGE_BYTES;
-    static constexpr int OFF_VEC = OFF_DS + DS_BYTES;  // NSQ x (lse2[128], delta[128])
+    static constexpr int OFF_VEC = OFF_STAGE + NSQ * STAGE_BYTES;  // NSQ x (lse2, delta)
     static constexpr int OFF_BAR = OFF_VEC + NSQ * 1024;
     static constexpr int BAR_BYTES = 256;
     static constexpr int LAYOUT_BYTES = OFF_BAR + BAR_BYTES;
@@ -73,7 +71,7 @@ struct BwdCfg {
     static_assert(LAYOUT_BYTES <= kMaxDynSmem, "backward tiles do not fit in shared memory");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
-    static constexpr int THREADS = 320;
+    static constexpr int THREADS = 352;
     static constexpr int COMPUTE_WARPS = 8;
 };
 
@@ -81,25 +79,22 @@ template <int NSQ>
 struct BwdBars {
     static constexpr int KV_FULL = 0;
     static constexpr int Q_FULL = 1;
-    static constexpr int S_FULL = Q_FULL + NSQ;
+    static constexpr int Q_EMPTY = Q_FULL + NSQ;
+    static constexpr int S_FULL = Q_EMPTY + NSQ;
     static constexpr int DP_FULL = S_FULL + 1;
     static constexpr int P_FULL = DP_FULL + 1;
     static constexpr int DS_FULL = P_FULL + 1;
-    static constexpr int DQ_FULL = DS_FULL + 1;
-    static constexpr int DQ_EMPTY = DQ_FULL + 1;
-    static constexpr int DQ_STAGED = DQ_EMPTY + 1;
-    static constexpr int ACC_FULL = DQ_STAGED + 1;
+    static constexpr int ACC_FULL = DS_FULL + 1;
     static constexpr int DONE = ACC_FULL + 1;
     static constexpr int COUNT = DONE + 1;
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     bwd_dkdv_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_do,
-                         const __grid_constant__ CUtensorMap tm_dq,
                          const float* __restrict__ delta, const float* __restrict__ lse2,
                          float* __restrict__ dk, float* __restrict__ dv, int N, int n_pad,
                          int BH, int n_tiles, int group, float scale, float scale_log2,
@@ -118,7 +113,6 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t s_k = s_base + C::OFF_K;
     const uint32_t s_v = s_base + C::OFF_V;
     const uint32_t s_stage = s_base + C::OFF_STAGE;
-    const uint32_t s_ds = s_base + C::OFF_DS;
     const uint32_t s_vec = s_base + C::OFF_VEC;
     const uint32_t s_bar = s_base + C::OFF_BAR;
     auto bar = [&](int slot) -> uint32_t { return s_bar + 8u * static_cast<uint32_t>(slot); };
@@ -128,7 +122,7 @@ __global__ void __launch_bounds__(320, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     // Key tile 0 sees every Q tile under a causal mask: heavy tiles first,
-    // a few heads at a time so their Q, dO and dq stay in L2.
+    // a few heads at a time so their Q and dO stay in L2.
     const long long lin = blockIdx.x + static_cast<long long>(gridDim.x) *
                                            (blockIdx.y + static_cast<long long>(gridDim.y) *
                                                              blockIdx.z);
@@ -143,23 +137,22 @@ __global__ void __launch_bounds__(320, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(Bar::KV_FULL), 1);
-        for (int s = 0; s < C::NSQ; ++s) mbar_init(bar(Bar::Q_FULL + s), 1);
+        for (int s = 0; s < C::NSQ; ++s) {
+            mbar_init(bar(Bar::Q_FULL + s), 1);
+            mbar_init(bar(Bar::Q_EMPTY + s), 2);  // one commit per issuer
+        }
         mbar_init(bar(Bar::S_FULL), 1);
         mbar_init(bar(Bar::DP_FULL), 1);
         mbar_init(bar(Bar::P_FULL), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::DS_FULL), C::COMPUTE_WARPS);
-        mbar_init(bar(Bar::DQ_FULL), 1);
-        mbar_init(bar(Bar::DQ_EMPTY), C::COMPUTE_WARPS);
-        mbar_init(bar(Bar::DQ_STAGED), C::COMPUTE_WARPS);
-        mbar_init(bar(Bar::ACC_FULL), 1);
-        mbar_init(bar(Bar::DONE), 1);
+        mbar_init(bar(Bar::ACC_FULL), 2);
+        mbar_init(bar(Bar::DONE), 2);
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_do);
-        prefetch_tensormap(&tm_dq);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -197,102 +190,80 @@ __global__ void __launch_bounds__(320, 1)
                             kt * C::BN, bh);
             }
             int issued = 0;
-            for (; issued < n_q && issued < C::NSQ; ++issued) load_tile(issued);
-            for (int t = 0; t < n_q; ++t) {
-                const int st = t % C::NSQ;
-                if (!mbar_wait(bar(Bar::DQ_STAGED), t & 1, wc)) break;
-                // dQ_t sits in stage st in the dq map's box layout: add it into dq.
-                for (int b = 0; b < D / 32; ++b)
-                    tma_reduce_add_3d(&tm_dq, q_of(st) + b * C::BOX_BYTES, b * 32,
-                                      (i0 + t) * C::BM, bh);
-                bulk_commit();
-                bulk_wait_read_all();
-                if (issued < n_q) load_tile(issued++);
+            for (; issued < n_q; ++issued) {
+                const int use = issued / C::NSQ;
+                if (use > 0 &&
+                    !mbar_wait(bar(Bar::Q_EMPTY + issued % C::NSQ), (use - 1) & 1, wc))
+                    break;
+                load_tile(issued);
             }
-            bulk_wait_all();
             mbar_wait_drain(bar(Bar::KV_FULL), 0, timeout_ns);
             for (int t = (issued > C::NSQ ? issued - C::NSQ : 0); t < issued; ++t)
                 mbar_wait_drain(bar(Bar::Q_FULL + t % C::NSQ), (t / C::NSQ) & 1, timeout_ns);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 10) {
+        // ------------------------------------------------------------ MMA issuers
         if (lane == 0) {
             constexpr uint32_t id_sp = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
             constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);    // dV, dK: B MN-major
-            constexpr uint32_t id_q = idesc_bf16(128, D, 1, 1);     // dQ: A and B MN-major
-            auto issue_s = [&](int t) -> bool {  // S^T_t = K Q_t^T
+            const bool issuer_a = (warp == 1);
+            // Base descriptors; each MMA below only moves the start address.
+            const uint64_t d_k = smem_desc_sw128(s_k, 16, 1024);                // A of S^T
+            const uint64_t d_v = smem_desc_sw128(s_v, 16, 1024);                // A of dP^T
+            // Stage 0 descriptors; stage st sits st * STAGE_BYTES further on.
+            // issuer A: Q (K-major, B of S^T) and dO (MN-major, B of dV);
+            // issuer B: dO (K-major, B of dP^T) and Q (MN-major, B of dK).
+            const uint64_t d_kmaj0 = smem_desc_sw128(issuer_a ? q_of(0) : do_of(0), 16, 1024);
+            const uint64_t d_mn0 = smem_desc_sw128(issuer_a ? do_of(0) : q_of(0), C::BOX_BYTES, 1024);
+            const uint64_t d_first = issuer_a ? d_k : d_v;
+            const uint32_t c_first = issuer_a ? C::COL_S : C::COL_DP;   // S^T or dP^T
+            const uint32_t c_acc = issuer_a ? C::COL_DV : C::COL_DK;    // dV or dK
+            const uint32_t c_a = issuer_a ? C::COL_S : C::COL_DP;       // P^T or dS^T
+            const int ready_bar = issuer_a ? Bar::P_FULL : Bar::DS_FULL;
+            const int full_bar = issuer_a ? Bar::S_FULL : Bar::DP_FULL;
+            // First GEMM of tile t: S^T_t = K Q_t^T (A) or dP^T_t = V dO_t^T (B).
+            auto issue_first = [&](int t) -> bool {
                 const int st = t % C::NSQ;
                 if (!mbar_wait(bar(Bar::Q_FULL + st), (t / C::NSQ) & 1, wc)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                    mma_ss(tmem + C::COL_S, smem_desc_sw128(s_k + koff, 16, 1024),
-                           smem_desc_sw128(q_of(st) + koff, 16, 1024), id_sp, kk > 0);
+                    mma_ss(tmem + c_first, desc_advance(d_first, koff),
+                           desc_advance(d_kmaj0, st * C::STAGE_BYTES + koff), id_sp, kk > 0);
                 }
-                tc_commit(bar(Bar::S_FULL));
+                tc_commit(bar(full_bar));
                 return true;
             };
-            bool ok = mbar_wait(bar(Bar::KV_FULL), 0, wc) && issue_s(0);
+            bool ok = mbar_wait(bar(Bar::KV_FULL), 0, wc) && issue_first(0);
             for (int t = 0; t < n_q && ok; ++t) {
                 const int st = t % C::NSQ;
-                if (t > 0) {  // dQ_{t-1} must be out of the DP columns
-                    ok = mbar_wait(bar(Bar::DQ_EMPTY), (t - 1) & 1, wc);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO_t^T
-                    const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                    mma_ss(tmem + C::COL_DP, smem_desc_sw128(s_v + koff, 16, 1024),
-                           smem_desc_sw128(do_of(st) + koff, 16, 1024), id_sp, kk > 0);
-                }
-                tc_commit(bar(Bar::DP_FULL));
-                const uint32_t acc = (t > 0) ? 1u : 0u;
-                ok = mbar_wait(bar(Bar::P_FULL), t & 1, wc);
+                ok = mbar_wait(bar(ready_bar), t & 1, wc);
                 if (!ok) break;
                 tc_fence_after();
+                // dV += P^T_t dO_t (A) or dK += dS^T_t Q_t (B); the BF16 halves
+                // of P^T / dS^T (queries 0-63, 64-127) sit at columns [0,32) and
+                // [64,96) of their fp32 region.
 #pragma unroll
-                for (int kk = 0; kk < C::BM / 16; ++kk) {  // dV += P^T dO_t
-                    // P^T halves: queries 0-63 at columns [0,32), 64-127 at [64,96).
-                    const uint32_t pcol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-                    mma_ts(tmem + C::COL_DV, tmem + C::COL_S + pcol,
-                           smem_desc_sw128(do_of(st) + kk * 2048, C::BOX_BYTES, 1024), id_kv,
-                           acc | (kk > 0));
+                for (int kk = 0; kk < C::BM / 16; ++kk) {
+                    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                    mma_ts(tmem + c_acc, tmem + c_a + acol, desc_advance(d_mn0, st * C::STAGE_BYTES + kk * 2048),
+                           id_kv, (t > 0 || kk > 0) ? 1u : 0u);
                 }
-                if (t + 1 < n_q) {
-                    ok = issue_s(t + 1);
-                    if (!ok) break;
-                }
-                ok = mbar_wait(bar(Bar::DS_FULL), t & 1, wc);
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < C::BM / 16; ++kk)  // dK += dS^T Q_t
-                    mma_ss(tmem + C::COL_DK,
-                           smem_desc_sw128(s_ds + (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32, 16,
-                                           1024),
-                           smem_desc_sw128(q_of(st) + kk * 2048, C::BOX_BYTES, 1024), id_kv,
-                           acc | (kk > 0));
-#pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)  // dQ_t = dS K
-                    mma_ss(tmem + C::COL_DP,
-                           smem_desc_sw128(s_ds + kk * 2048, C::BOX_BYTES, 1024),
-                           smem_desc_sw128(s_k + kk * 2048, C::BOX_BYTES, 1024), id_q, kk > 0);
-                tc_commit(bar(Bar::DQ_FULL));
+                tc_commit(bar(Bar::Q_EMPTY + st));  // this issuer no longer reads stage t
+                if (t + 1 < n_q) ok = issue_first(t + 1);
             }
             if (ok) tc_commit(bar(Bar::ACC_FULL));
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ P / dS / dQ
+        // ------------------------------------------------------------ P / dS
         const int wq = warp & 3;
         const int h = (warp - 2) >> 2;       // column half
-        const int r = wq * 32 + lane;        // key row (query row in phase dQ)
+        const int r = wq * 32 + lane;        // key row
         const int kglob = kt * C::BN + r;    // key index inside the head
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const float* vec_base = reinterpret_cast<const float*>(smem + C::OFF_VEC);
-        uint8_t* ds_box = smem + C::OFF_DS + h * C::BOX_BYTES;
         const bool key_pad = kglob >= N;
         bool ok = true;
         for (int t = 0; t < n_q; ++t) {
@@ -335,58 +306,26 @@ __global__ void __launch_bounds__(320, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(Bar::P_FULL));
 
-            // Phase dS: dS^T = P o (dP^T - D) * scale into smem box h, row r.
+            // Phase dS: dS^T = P o (dP^T - D) * scale, BF16, over its dP^T columns.
             ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DP_FULL), t & 1, wc));
             if (!ok) break;
             tc_fence_after();
             {
                 uint32_t dr[64];
                 tmem_ld64(t_lane + C::COL_DP + 64 * h, dr);
+                uint32_t w[32];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 8 * u + 2 * e;
-                        w[e] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - dlt[c]) * scale,
-                                           p[c + 1] * (__uint_as_float(dr[c + 1]) - dlt[c + 1]) *
-                                               scale);
-                    }
-                    *reinterpret_cast<uint4*>(ds_box + r * 128 + ((u ^ (r & 7)) * 16)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 32; ++e) {
+                    const int c = 2 * e;
+                    w[e] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - dlt[c]),
+                                       p[c + 1] * (__uint_as_float(dr[c + 1]) - dlt[c + 1]));
                 }
+                tmem_st32(t_lane + C::COL_DP + 64 * h, w);
             }
-            fence_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(Bar::DS_FULL));
-
-            // Phase dQ: half h of query row r of dQ_t into stage st, box layout
-            // of the dq tensor map (128 rows x 32 fp32, 128-byte swizzle).
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DQ_FULL), t & 1, wc));
-            if (!ok) break;
-            tc_fence_after();
-            uint8_t* stage = smem + C::OFF_STAGE + st * C::STAGE_BYTES;
-#pragma unroll
-            for (int bb = 0; bb < D / 64; ++bb) {
-                uint32_t qr[32];
-                tmem_ld32(t_lane + C::COL_DP + (D / 2) * h + 32 * bb, qr);
-                if (bb == D / 64 - 1) {
-                    // Every dQ column of this lane is in registers: free the DP
-                    // columns for the next dP^T.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(Bar::DQ_EMPTY));
-                }
-                uint8_t* box = stage + ((D / 64) * h + bb) * C::BOX_BYTES + r * 128;
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<uint4*>(box + ((u ^ (r & 7)) * 16)) =
-                        make_uint4(qr[4 * u], qr[4 * u + 1], qr[4 * u + 2], qr[4 * u + 3]);
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Bar::DQ_STAGED));
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::ACC_FULL), 0, wc));
         if (ok) {
@@ -405,10 +344,10 @@ __global__ void __launch_bounds__(320, 1)
                             make_float4(__uint_as_float(a[4 * u]), __uint_as_float(a[4 * u + 1]),
                                         __uint_as_float(a[4 * u + 2]),
                                         __uint_as_float(a[4 * u + 3]));
-                        dk_row[ch * 8 + u] =
-                            make_float4(__uint_as_float(b[4 * u]), __uint_as_float(b[4 * u + 1]),
-                                        __uint_as_float(b[4 * u + 2]),
-                                        __uint_as_float(b[4 * u + 3]));
+                        dk_row[ch * 8 + u] = make_float4(
+                            __uint_as_float(b[4 * u]) * scale, __uint_as_float(b[4 * u + 1]) * scale,
+                            __uint_as_float(b[4 * u + 2]) * scale,
+                            __uint_as_float(b[4 * u + 3]) * scale);
                     }
                 }
             }
@@ -417,9 +356,10 @@ __global__ void __launch_bounds__(320, 1)
 
     // ---------------------------------------------------------------- teardown
     __syncthreads();
+    if (warp == 10 && lane == 0) tc_commit(bar(Bar::DONE));
     if (warp == 1) {
         if (lane == 0) {
-            tc_commit(bar(Bar::DONE));
+            tc_commit(bar(Bar::DONE));  // both issuers' MMAs have completed
             mbar_wait_drain(bar(Bar::DONE), 0, timeout_ns);
         }
         __syncwarp();
@@ -441,8 +381,8 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     if (group < 1) group = 1;
     dim3 grid(n_tiles, a.H, a.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, a.delta, a.lse2, a.dk, a.dv, a.N,
-        a.n_pad, a.B * a.H, n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
+        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, a.delta, a.lse2, a.dk, a.dv, a.N, a.n_pad,
+        a.B * a.H, n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
     return cudaGetLastError();
 }
 

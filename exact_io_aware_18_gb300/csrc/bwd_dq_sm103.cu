@@ -1,0 +1,378 @@
+// bwd_dq_sm103.cu - attention backward, dQ kernel, BF16 in / FP32 out,
+// tcgen05 + TMEM + TMA on sm_103a.
+//
+// Method.  dQ = scale dS K with dS = P o (dP - D), P = exp(scale Q K^T - LSE)
+// recomputed from the saved LSE ("Flash Attention: Revolutionizing
+// Transformer Efficiency", section "The Flash Attention algorithm", idea 2,
+// recomputation) and dP = dO V^T.  One CTA owns one 128-row Q tile of one
+// (b, h) and loops over the key tiles it sees (j <= i when causal), exactly
+// like the forward's loop order ("FlashAttention scaling, multi-GPU training
+// and weight quantization", section 1): the dQ tile accumulates in TMEM and is
+// written once, so the result does not depend on the order in which CTAs run
+// (no atomics; "FlashAttention-2" stresses a deterministic exact result).
+//
+// Roles (352 threads, one CTA per SM):
+//   warp 0      TMA producers: lane 0 loads Q_i and dO_i once, then K_j into a
+//               three-deep ring (K_j is read until the dQ MMA of tile j);
+//               lane 1 loads V_j into a two-deep ring (read only by dP_j).
+//               The two rings free at different times, so each has its own
+//               thread and neither load waits behind the other's slot.
+//   warps 1, 10 two MMA issuers (one thread each; one thread alone issues a
+//               128 x 128 x 16 MMA no faster than the pipe runs it, so its
+//               barrier checks would idle the pipe).  Issuer A: S_0, S_1, then
+//               per key tile j: dQ += dS_j K_j (A = dS_j in TMEM, after
+//               DS_FULL) and S_j+2 = Q K_j+2^T over dS_j.  Issuer B: dP_0, then
+//               dP_j+1 = dO V_j+1^T as soon as the math warps hold dP_j in
+//               registers.  S is double buffered and dP is released early, so
+//               both operands of tile j+1 are ready when the math of tile j
+//               ends.
+//   warps 2..9  thread (r, h) owns query row r (TMEM lane r) and key half h:
+//               P' = exp2(S * scale*log2e - LSE2_r + log2 scale) = scale P,
+//               dS' = P' o (dP - D_r) = scale dS, BF16, written over the first
+//               32 of its own 64 S columns.  At the end: the dQ row half out
+//               of TMEM to global memory (FP32).
+// TMEM columns: S buffers [0,128) and [128,256), dP [256,384), dQ [384,384+d).
+// All waits are bounded (see sm103_primitives.cuh).
+#include "fa_internal.h"
+#include "sm103_primitives.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kMaxDynSmem = 232448;  // 227 KB opt-in limit per block
+
+template <int D>
+struct DqCfg {
+    static constexpr int BM = 128;  // query rows per CTA
+    static constexpr int BN = 128;  // keys per tile
+    static constexpr int KB = D / 64;
+    static constexpr int BOX_BYTES = 128 * 64 * 2;
+    static constexpr int TILE_BYTES = KB * BOX_BYTES;
+    static constexpr int NSK = 3;  // K ring depth
+    static constexpr int NSV = 2;  // V ring depth
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_DO = OFF_Q + TILE_BYTES;
+    static constexpr int OFF_K = OFF_DO + TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_V + NSV * TILE_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int LAYOUT_BYTES = OFF_BAR + BAR_BYTES;
+    static constexpr int SMEM_BYTES =
+        (LAYOUT_BYTES + 1024 <= kMaxDynSmem) ? LAYOUT_BYTES + 1024 : kMaxDynSmem;
+    static_assert(LAYOUT_BYTES <= kMaxDynSmem, "dQ tiles do not fit in shared memory");
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_DP = 256, COL_DQ = 384;
+    static constexpr int THREADS = 352;
+    static constexpr int COMPUTE_WARPS = 8;
+};
+
+template <int NSK, int NSV>
+struct DqBars {
+    static constexpr int QD_FULL = 0;
+    static constexpr int K_FULL = 1;
+    static constexpr int K_EMPTY = K_FULL + NSK;
+    static constexpr int V_FULL = K_EMPTY + NSK;
+    static constexpr int V_EMPTY = V_FULL + NSV;
+    static constexpr int S_FULL = V_EMPTY + NSV;  // 2
+    static constexpr int DP_FULL = S_FULL + 2;
+    static constexpr int DP_EMPTY = DP_FULL + 1;
+    static constexpr int DS_FULL = DP_EMPTY + 1;
+    static constexpr int DQ_DONE = DS_FULL + 1;
+    static constexpr int DONE = DQ_DONE + 1;
+    static constexpr int COUNT = DONE + 1;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(352, 1)
+    bwd_dq_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_do,
+                       const float* __restrict__ delta, const float* __restrict__ lse2,
+                       float* __restrict__ dq, int N, int n_pad, int BH, int n_tiles, int group,
+                       float scale, float scale_log2, unsigned int* status,
+                       unsigned long long timeout_ns) {
+    using C = DqCfg<D>;
+    using Bar = DqBars<C::NSK, C::NSV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    if (smem + C::LAYOUT_BYTES > smem_raw + C::SMEM_BYTES) {
+        if (threadIdx.x == 0) atomicOr(status, kStatusSmemLayout);
+        return;
+    }
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t s_q = s_base + C::OFF_Q;
+    const uint32_t s_do = s_base + C::OFF_DO;
+    const uint32_t s_k = s_base + C::OFF_K;
+    const uint32_t s_v = s_base + C::OFF_V;
+    const uint32_t s_bar = s_base + C::OFF_BAR;
+    auto bar = [&](int slot) -> uint32_t { return s_bar + 8u * static_cast<uint32_t>(slot); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * Bar::COUNT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    // Heavy Q tiles first (the last Q tile sees the most keys under a causal
+    // mask), a few heads at a time so that their K and V stay in L2.
+    const long long lin = blockIdx.x + static_cast<long long>(gridDim.x) *
+                                           (blockIdx.y + static_cast<long long>(gridDim.y) *
+                                                             blockIdx.z);
+    const TileHead th = grouped_order(lin, BH, n_tiles, group, true);
+    const int qt = th.tile;
+    const int bh = th.head;
+    const int n_kv = CAUSAL ? qt + 1 : n_tiles;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(Bar::QD_FULL), 1);
+        for (int s = 0; s < C::NSK; ++s) {
+            mbar_init(bar(Bar::K_FULL + s), 1);
+            mbar_init(bar(Bar::K_EMPTY + s), 1);
+        }
+        for (int s = 0; s < C::NSV; ++s) {
+            mbar_init(bar(Bar::V_FULL + s), 1);
+            mbar_init(bar(Bar::V_EMPTY + s), 1);
+        }
+        mbar_init(bar(Bar::S_FULL), 1);
+        mbar_init(bar(Bar::S_FULL + 1), 1);
+        mbar_init(bar(Bar::DP_FULL), 1);
+        mbar_init(bar(Bar::DP_EMPTY), C::COMPUTE_WARPS);
+        mbar_init(bar(Bar::DS_FULL), C::COMPUTE_WARPS);
+        mbar_init(bar(Bar::DQ_DONE), 1);
+        mbar_init(bar(Bar::DONE), 2);
+        *abort_flag = 0;
+        mbar_fence_init();
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_do);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const WaitCtx wc{status, timeout_ns, abort_flag};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producers
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(Bar::QD_FULL), 2 * C::TILE_BYTES);
+            for (int kb = 0; kb < C::KB; ++kb) {
+                tma_load_3d(s_q + kb * C::BOX_BYTES, &tm_q, bar(Bar::QD_FULL), kb * 64,
+                            qt * C::BM, bh);
+                tma_load_3d(s_do + kb * C::BOX_BYTES, &tm_do, bar(Bar::QD_FULL), kb * 64,
+                            qt * C::BM, bh);
+            }
+            int issued = 0;
+            for (; issued < n_kv; ++issued) {
+                const int st = issued % C::NSK, use = issued / C::NSK;
+                if (use > 0 && !mbar_wait(bar(Bar::K_EMPTY + st), (use - 1) & 1, wc)) break;
+                mbar_arrive_expect_tx(bar(Bar::K_FULL + st), C::TILE_BYTES);
+                for (int kb = 0; kb < C::KB; ++kb)
+                    tma_load_3d(s_k + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_k,
+                                bar(Bar::K_FULL + st), kb * 64, issued * C::BN, bh);
+            }
+            mbar_wait_drain(bar(Bar::QD_FULL), 0, timeout_ns);
+            for (int j = (issued > C::NSK ? issued - C::NSK : 0); j < issued; ++j)
+                mbar_wait_drain(bar(Bar::K_FULL + j % C::NSK), (j / C::NSK) & 1, timeout_ns);
+        } else if (lane == 1) {
+            int issued = 0;
+            for (; issued < n_kv; ++issued) {
+                const int st = issued % C::NSV, use = issued / C::NSV;
+                if (use > 0 && !mbar_wait(bar(Bar::V_EMPTY + st), (use - 1) & 1, wc)) break;
+                mbar_arrive_expect_tx(bar(Bar::V_FULL + st), C::TILE_BYTES);
+                for (int kb = 0; kb < C::KB; ++kb)
+                    tma_load_3d(s_v + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_v,
+                                bar(Bar::V_FULL + st), kb * 64, issued * C::BN, bh);
+            }
+            for (int j = (issued > C::NSV ? issued - C::NSV : 0); j < issued; ++j)
+                mbar_wait_drain(bar(Bar::V_FULL + j % C::NSV), (j / C::NSV) & 1, timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer A
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // S: both K-major
+            constexpr uint32_t id_q = idesc_bf16(128, D, 0, 1);    // dQ: B MN-major
+            const uint64_t d_q = smem_desc_sw128(s_q, 16, 1024);
+            const uint64_t d_kk = smem_desc_sw128(s_k, 16, 1024);            // K, K-major
+            const uint64_t d_kmn = smem_desc_sw128(s_k, C::BOX_BYTES, 1024);  // K, MN-major
+            auto issue_s = [&](int j) -> bool {  // S_j = Q K_j^T into buffer j & 1
+                const int st = j % C::NSK;
+                if (!mbar_wait(bar(Bar::K_FULL + st), (j / C::NSK) & 1, wc)) return false;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                    mma_ss(d_tmem, desc_advance(d_q, koff),
+                           desc_advance(d_kk, st * C::TILE_BYTES + koff), id_s, kk > 0);
+                }
+                tc_commit(bar(Bar::S_FULL + (j & 1)));
+                return true;
+            };
+            bool ok = mbar_wait(bar(Bar::QD_FULL), 0, wc) && issue_s(0);
+            if (ok && n_kv > 1) ok = issue_s(1);
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int st = j % C::NSK;
+                ok = mbar_wait(bar(Bar::DS_FULL), j & 1, wc);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t s_cols = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk) {  // dQ += dS_j K_j
+                    // dS halves: keys 0-63 at columns [0,32), 64-127 at [64,96).
+                    const uint32_t scol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                    mma_ts(tmem + C::COL_DQ, s_cols + scol,
+                           desc_advance(d_kmn, st * C::TILE_BYTES + kk * 2048), id_q,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(Bar::K_EMPTY + st));
+                if (j + 2 < n_kv) ok = issue_s(j + 2);
+            }
+            if (ok) tc_commit(bar(Bar::DQ_DONE));
+        }
+        __syncwarp();
+    } else if (warp == 10) {
+        // ------------------------------------------------------------ MMA issuer B
+        if (lane == 0) {
+            constexpr uint32_t id_p = idesc_bf16(128, 128, 0, 0);  // dP: both K-major
+            const uint64_t d_do = smem_desc_sw128(s_do, 16, 1024);
+            const uint64_t d_vv = smem_desc_sw128(s_v, 16, 1024);
+            auto issue_dp = [&](int j) -> bool {  // dP_j = dO V_j^T
+                const int st = j % C::NSV;
+                if (!mbar_wait(bar(Bar::V_FULL + st), (j / C::NSV) & 1, wc)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                    mma_ss(tmem + C::COL_DP, desc_advance(d_do, koff),
+                           desc_advance(d_vv, st * C::TILE_BYTES + koff), id_p, kk > 0);
+                }
+                tc_commit(bar(Bar::V_EMPTY + st));
+                tc_commit(bar(Bar::DP_FULL));
+                return true;
+            };
+            bool ok = mbar_wait(bar(Bar::QD_FULL), 0, wc) && issue_dp(0);
+            for (int j = 0; j + 1 < n_kv && ok; ++j)  // the math warps hold dP_j in registers
+                ok = mbar_wait(bar(Bar::DP_EMPTY), j & 1, wc) && issue_dp(j + 1);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ P / dS
+        const int wq = warp & 3;
+        const int h = (warp - 2) >> 2;       // key half
+        const int r = wq * 32 + lane;        // query row
+        const int qglob = qt * C::BM + r;    // query index inside the head
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const long long voff = static_cast<long long>(bh) * n_pad + qt * C::BM + r;
+        // +inf on padding rows, so P = 0 there; log2(scale) folds scale into P.
+        const float neg_l2 = log2f(scale) - lse2[voff];
+        const float d_r = delta[voff];
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            const uint32_t t_s = t_lane + ((j & 1) ? C::COL_S1 : C::COL_S0) + 64 * h;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_FULL + (j & 1)), (j >> 1) & 1, wc) &&
+                                             mbar_wait(bar(Bar::DP_FULL), j & 1, wc));
+            if (!ok) break;
+            tc_fence_after();
+            const int key0 = j * C::BN + 64 * h;  // key index of entry 0
+            const bool masked = (CAUSAL && j == qt) || key0 + 64 > N;
+            // dP_j into registers first, so the next dP can be computed meanwhile.
+            uint32_t dr[64];
+            tmem_ld64(t_lane + C::COL_DP + 64 * h, dr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Bar::DP_EMPTY));
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {  // two chunks of 32 keys
+                uint32_t sr[32], w[16];
+                tmem_ld32(t_s + 32 * ch, sr);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int c = 2 * e + u;
+                        float p = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, neg_l2));
+                        if (masked) {
+                            const int key = key0 + 32 * ch + c;
+                            if ((CAUSAL && key > qglob) || key >= N) p = 0.f;
+                        }
+                        ds[u] = p * (__uint_as_float(dr[32 * ch + c]) - d_r);
+                    }
+                    w[e] = pack_bf16x2(ds[0], ds[1]);
+                }
+                // Chunk ch's dS lands on S columns [16 ch, 16 ch + 16) of this
+                // half, which chunk 0 has already read.
+                tmem_st16(t_s + 16 * ch, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Bar::DS_FULL));
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DQ_DONE), 0, wc));
+        if (ok) {
+            tc_fence_after();
+            float4* dq_row = reinterpret_cast<float4*>(
+                dq + (static_cast<long long>(bh) * N + qglob) * D + (D / 2) * h);
+#pragma unroll
+            for (int ch = 0; ch < D / 64; ++ch) {
+                uint32_t a[32];
+                tmem_ld32(t_lane + C::COL_DQ + (D / 2) * h + ch * 32, a);
+                if (qglob < N) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        dq_row[ch * 8 + u] =
+                            make_float4(__uint_as_float(a[4 * u]), __uint_as_float(a[4 * u + 1]),
+                                        __uint_as_float(a[4 * u + 2]),
+                                        __uint_as_float(a[4 * u + 3]));
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    __syncthreads();
+    if (warp == 10 && lane == 0) tc_commit(bar(Bar::DONE));
+    if (warp == 1) {
+        if (lane == 0) {
+            tc_commit(bar(Bar::DONE));  // both issuers' MMAs have completed
+            mbar_wait_drain(bar(Bar::DONE), 0, timeout_ns);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_t(const DqArgs& a, cudaStream_t stream) {
+    using C = DqCfg<D>;
+    auto kern = bwd_dq_bf16_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int n_tiles = (a.N + C::BM - 1) / C::BM;
+    int group = 128 / n_tiles;
+    if (group < 1) group = 1;
+    dim3 grid(n_tiles, a.H, a.B);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
+        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, a.delta, a.lse2, a.dq, a.N, a.n_pad, a.B * a.H,
+        n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq_bf16(const DqArgs& a, cudaStream_t stream) {
+    if (a.d == 64) return a.causal ? launch_t<64, true>(a, stream) : launch_t<64, false>(a, stream);
+    return a.causal ? launch_t<128, true>(a, stream) : launch_t<128, false>(a, stream);
+}
+
+}  // namespace fa

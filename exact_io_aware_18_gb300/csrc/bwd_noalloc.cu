@@ -73,8 +73,10 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
     const size_t half = need / (2 * sizeof(float));  // B*H*roundup(N,128) floats
     float* delta = scratch;
     float* lse2 = scratch + half;
-    int rc = fa_bwd_preprocess(o, do_, lse, delta, lse2, dq, B, H, N, d, stream);
-    if (rc != FA_OK) return rc;
-    return fa_bwd_dkdv(q, k, v, do_, delta, lse2, dq, dk, dv, B, H, N, d, causal, scale,
-                       stream);
+    int rc = fa_bwd_preprocess(o, do_, lse, delta, lse2, B, H, N, d, stream);
+    if (rc == FA_OK)
+        rc = fa_bwd_dkdv(q, k, v, do_, delta, lse2, dk, dv, B, H, N, d, causal, scale, stream);
+    if (rc == FA_OK)
+        rc = fa_bwd_dq(q, k, v, do_, delta, lse2, dq, B, H, N, d, causal, scale, stream);
+    return rc;
 }

@@ -5,13 +5,12 @@
 //   delta[i] = D_i = sum_c dO_ic O_ic     (0 on padding rows)
 //   lse2[i]  = LSE_i * log2(e)            (+inf on padding rows, so that the
 //                                          recomputed P of a padding row is 0)
-//   dq[i, :] = 0                          (dQ is then accumulated with atomics)
 // D is the row term of the softmax gradient dS = P o (dP - D); P itself is
 // recomputed later from LSE ("Flash Attention: Revolutionizing Transformer
 // Efficiency", section "The Flash Attention algorithm", recomputation).
 //
-// Each thread moves 16-byte vectors: 8 bf16 of O and of dO in, 8 fp32 zeros of
-// dq out; d/8 threads share a row and reduce with warp shuffles.  The grid is
+// Each thread reads 16-byte vectors, 8 bf16 of O and of dO; d/8 threads share
+// a row and reduce with warp shuffles.  The grid is
 // a multiple of the SM count with a grid-stride loop over rows.
 #include <cuda_bf16.h>
 
@@ -27,7 +26,7 @@ template <int D>
 __global__ void __launch_bounds__(kPreThreads)
     bwd_pre_bf16_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
                         const float* __restrict__ lse, float* __restrict__ delta,
-                        float* __restrict__ lse2, float4* __restrict__ dq, int N, int n_pad,
+                        float* __restrict__ lse2, int N, int n_pad,
                         long long total_rows) {
     constexpr int TPR = D / 8;                  // threads per row
     constexpr int RPB = kPreThreads / TPR;      // rows per block per pass
@@ -51,9 +50,6 @@ __global__ void __launch_bounds__(kPreThreads)
                 part = fmaf(x.x, y.x, part);
                 part = fmaf(x.y, y.y, part);
             }
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            dq[row * (D / 4) + 2 * sub] = z;
-            dq[row * (D / 4) + 2 * sub + 1] = z;
         }
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1)
@@ -93,11 +89,11 @@ cudaError_t launch_bwd_pre_bf16(const BwdPreArgs& a, cudaStream_t stream) {
     if (a.d == 64)
         bwd_pre_bf16_kernel<64><<<static_cast<int>(blocks), kPreThreads, 0, stream>>>(
             static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.lse, a.delta,
-            a.lse2, reinterpret_cast<float4*>(a.dq), a.N, a.n_pad, total);
+            a.lse2, a.N, a.n_pad, total);
     else
         bwd_pre_bf16_kernel<128><<<static_cast<int>(blocks), kPreThreads, 0, stream>>>(
             static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.lse, a.delta,
-            a.lse2, reinterpret_cast<float4*>(a.dq), a.N, a.n_pad, total);
+            a.lse2, a.N, a.n_pad, total);
     return cudaGetLastError();
 }
 

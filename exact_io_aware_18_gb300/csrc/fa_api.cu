@@ -78,24 +78,6 @@ int make_map_bf16(CUtensorMap* map, const void* ptr, int d, int N, long long BH)
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// [B*H, N, d] fp32 viewed as (d, N, B*H); 128-row x 32-column boxes (128
-// bytes wide, 128-byte swizzle): the dQ bulk-reduction target.
-int make_map_f32(CUtensorMap* map, const void* ptr, int d, int N, long long BH) {
-    EncodeFn enc;
-    if (int rc = get_encode(&enc)) return rc;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                          static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
-                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 4};
-    cuuint32_t box[3] = {32, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(int B, int H, int N, int d, float scale) {
@@ -179,32 +161,50 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
 }
 
 int fa_bwd_preprocess(const void* o, const void* do_, const float* lse, float* delta_ws,
-                      float* lse2_ws, float* dq, int B, int H, int N, int d, void* stream) {
-    if (int rc = check_ptrs({o, do_, lse, delta_ws, lse2_ws, dq})) return rc;
+                      float* lse2_ws, int B, int H, int N, int d, void* stream) {
+    if (int rc = check_ptrs({o, do_, lse, delta_ws, lse2_ws})) return rc;
     if (int rc = check_shape(B, H, N, d, 1.f)) return rc;
-    fa::BwdPreArgs a{o, do_, lse, delta_ws, lse2_ws, dq, B * H, N, d,
+    fa::BwdPreArgs a{o, do_, lse, delta_ws, lse2_ws, B * H, N, d,
                      static_cast<int>(n_pad_of(N))};
     return launch_rc(fa::launch_bwd_pre_bf16(a, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
-                const float* delta_ws, const float* lse2_ws, float* dq, float* dk, float* dv,
-                int B, int H, int N, int d, int causal, float scale, void* stream) {
-    if (int rc = check_ptrs({q, k, v, do_, delta_ws, lse2_ws, dq, dk, dv})) return rc;
+                const float* delta_ws, const float* lse2_ws, float* dk, float* dv, int B, int H,
+                int N, int d, int causal, float scale, void* stream) {
+    if (int rc = check_ptrs({q, k, v, do_, delta_ws, lse2_ws, dk, dv})) return rc;
     if (int rc = check_shape(B, H, N, d, scale)) return rc;
     unsigned int* status;
     if (int rc = status_ptr(&status)) return rc;
     const long long BH = static_cast<long long>(B) * H;
-    CUtensorMap tq, tk, tv, tdo, tdq;
+    CUtensorMap tq, tk, tv, tdo;
     if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
-    if (int rc = make_map_f32(&tdq, dq, d, N, BH)) return rc;
-    fa::BwdArgs a{&tq, &tk, &tv, &tdo, &tdq, delta_ws, lse2_ws, dk, dv, B, H, N, d,
+    fa::BwdArgs a{&tq, &tk, &tv, &tdo, delta_ws, lse2_ws, dk, dv, B, H, N, d,
                   static_cast<int>(n_pad_of(N)), causal ? 1 : 0, scale,
                   scale * 1.4426950408889634f, status, g_timeout_ns.load()};
     return launch_rc(fa::launch_bwd_dkdv_bf16(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_dq(const void* q, const void* k, const void* v, const void* do_,
+              const float* delta_ws, const float* lse2_ws, float* dq, int B, int H, int N, int d,
+              int causal, float scale, void* stream) {
+    if (int rc = check_ptrs({q, k, v, do_, delta_ws, lse2_ws, dq})) return rc;
+    if (int rc = check_shape(B, H, N, d, scale)) return rc;
+    unsigned int* status;
+    if (int rc = status_ptr(&status)) return rc;
+    const long long BH = static_cast<long long>(B) * H;
+    CUtensorMap tq, tk, tv, tdo;
+    if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
+    fa::DqArgs a{&tq, &tk, &tv, &tdo, delta_ws, lse2_ws, dq, B, H, N, d,
+                 static_cast<int>(n_pad_of(N)), causal ? 1 : 0, scale,
+                 scale * 1.4426950408889634f, status, g_timeout_ns.load()};
+    return launch_rc(fa::launch_bwd_dq_bf16(a, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_,
@@ -223,10 +223,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     }
     float* delta = static_cast<float*>(ws);
     float* lse2 = delta + static_cast<size_t>(B) * H * n_pad_of(N);
-    int rc = fa_bwd_preprocess(o, do_, lse, delta, lse2, dq, B, H, N, d, stream);
+    int rc = fa_bwd_preprocess(o, do_, lse, delta, lse2, B, H, N, d, stream);
     if (rc == FA_OK)
-        rc = fa_bwd_dkdv(q, k, v, do_, delta, lse2, dq, dk, dv, B, H, N, d, causal, scale,
-                         stream);
+        rc = fa_bwd_dkdv(q, k, v, do_, delta, lse2, dk, dv, B, H, N, d, causal, scale, stream);
+    if (rc == FA_OK)
+        rc = fa_bwd_dq(q, k, v, do_, delta, lse2, dq, B, H, N, d, causal, scale, stream);
     if (!workspace && cudaFreeAsync(ws, s) != cudaSuccess && rc == FA_OK) rc = FA_ERR_CUDA;
     return rc;
 }

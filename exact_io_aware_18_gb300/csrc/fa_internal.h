@@ -27,28 +27,24 @@ struct FwdArgs {
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);
 
 // Backward preprocess (BF16): D and base-2 LSE into padded [B*H, n_pad]
-// vectors, zero dq.
+// vectors.
 struct BwdPreArgs {
     const void* o;
     const void* dO;
     const float* lse;
     float* delta;
     float* lse2;
-    float* dq;
     int BH, N, d, n_pad;
 };
 
 cudaError_t launch_bwd_pre_bf16(const BwdPreArgs& a, cudaStream_t stream);
 
-// Backward dK/dV + dQ (BF16).  Tensor maps for Q, K, V, dO as for the
-// forward; tm_dq views dq as (d, N, B*H) fp32 in 128-row x 32-column boxes
-// (128-byte swizzle), the target of the dQ bulk reductions.
+// Backward dK/dV (BF16).  Tensor maps for Q, K, V, dO as for the forward.
 struct BwdArgs {
     const CUtensorMap* tm_q;
     const CUtensorMap* tm_k;
     const CUtensorMap* tm_v;
     const CUtensorMap* tm_do;
-    const CUtensorMap* tm_dq;
     const float* delta;
     const float* lse2;
     float* dk;
@@ -62,6 +58,25 @@ struct BwdArgs {
 };
 
 cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t stream);
+
+// Backward dQ (BF16): one CTA per Q tile, loop over key tiles, dq written once.
+struct DqArgs {
+    const CUtensorMap* tm_q;
+    const CUtensorMap* tm_k;
+    const CUtensorMap* tm_v;
+    const CUtensorMap* tm_do;
+    const float* delta;
+    const float* lse2;
+    float* dq;
+    int B, H, N, d, n_pad;
+    int causal;
+    float scale;
+    float scale_log2;
+    unsigned int* status;
+    unsigned long long timeout_ns;
+};
+
+cudaError_t launch_bwd_dq_bf16(const DqArgs& a, cudaStream_t stream);
 
 // FP32 SIMT twins.
 struct F32Args {

@@ -235,6 +235,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
            (2ull << 61);   // 128-byte swizzle
 }
 
+// Same descriptor with its start address moved by `bytes` (a multiple of
+// 16; the address field cannot overflow for shared-memory offsets < 256 KB).
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+    return desc + (bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16: BF16 A and B, FP32 accumulator, dense.
 // a_mn / b_mn select MN-major (1) instead of K-major (0) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {

@@ -84,8 +84,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                   16-byte aligned, or NULL: the library then allocates and
  *                   frees it on the stream (cudaMallocAsync / cudaFreeAsync).
  *
- * Runs fa_bwd_preprocess then fa_bwd_dkdv on the stream.  dq is reduced
- * with FP32 atomics, so its bits may differ from run to run within rounding. */
+ * Runs fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq on the stream.  Every
+ * gradient entry is one sum in a fixed order (no atomics), so repeated calls
+ * give identical bits. */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_,
            const float* lse, float* dq, float* dk, float* dv,
            int B, int H, int N, int d, int causal, float scale,
@@ -93,18 +94,28 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 
 /* First backward step.  delta_ws : float [B*H, roundup(N,128)] receives
  * D_i = sum_c dO_ic O_ic (0 on padding rows); lse2_ws (same shape) receives
- * LSE_i * log2(e) (+inf on padding rows); dq [B,H,N,d] is set to zero.
- * Memory-bound; d must be 64 or 128. */
+ * LSE_i * log2(e) (+inf on padding rows).  Memory-bound; d must be 64 or 128. */
 int fa_bwd_preprocess(const void* o, const void* do_, const float* lse, float* delta_ws,
-                      float* lse2_ws, float* dq, int B, int H, int N, int d, void* stream);
+                      float* lse2_ws, int B, int H, int N, int d, void* stream);
 
-/* Second backward step.  One CTA per 128-key K/V tile of one (b, h): it keeps
- * K, V and the dK, dV accumulators on chip and loops over the Q tiles that
- * see those keys, recomputing P from lse2_ws, and adds each dQ tile into dq
- * with FP32 atomics.  delta_ws / lse2_ws as written by fa_bwd_preprocess. */
+/* Second backward step, dK and dV.  One CTA per 128-key K/V tile of one
+ * (b, h): it keeps K, V and the dK, dV accumulators on chip and loops over
+ * the Q tiles that see those keys, recomputing P from lse2_ws ("Flash
+ * Attention: Revolutionizing Transformer Efficiency", section "The Flash
+ * Attention algorithm", recomputation; "FlashAttention-2", technical
+ * architecture, improvement 2, parallelism over the sequence).
+ * delta_ws / lse2_ws as written by fa_bwd_preprocess; dk, dv float [B,H,N,d]. */
 int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
-                const float* delta_ws, const float* lse2_ws, float* dq, float* dk, float* dv,
+                const float* delta_ws, const float* lse2_ws, float* dk, float* dv,
                 int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/* Third backward step, dQ.  One CTA per 128-row Q tile of one (b, h): it
+ * loops over the key tiles that Q tile sees (the forward's loop order),
+ * recomputes P and dP and accumulates dQ on chip, then writes each dq row
+ * once (float [B,H,N,d]).  Inputs as for fa_bwd_dkdv. */
+int fa_bwd_dq(const void* q, const void* k, const void* v, const void* do_,
+              const float* delta_ws, const float* lse2_ws, float* dq,
+              int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /* Size of the scratch array built into the library for fa_bwd_noalloc:
  * 8 MiB, i.e. B * H * roundup(N, 128) <= 1048576. */

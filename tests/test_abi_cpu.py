@@ -33,7 +33,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("fa_fwd", "fa_bwd", "fa_fwd_f32", "fa_bwd_f32", "fa_bwd_workspace_bytes",
-                 "fa_error_string", "fa_device_status", "fa_bwd_preprocess", "fa_bwd_dkdv"):
+                 "fa_error_string", "fa_device_status", "fa_bwd_preprocess", "fa_bwd_dkdv",
+                 "fa_bwd_dq"):
         assert must in names
 
 
@@ -90,8 +91,12 @@ def test_argument_checks_before_launch(fa):
     assert bwd == fa.FA_ERR_MISALIGNED
     bwd = lib.fa_bwd(*([0x10000] * 9), 1, 1, 16, 64, 0, 0.125, 0x20000, 16, None)
     assert bwd == fa.FA_ERR_NO_MEMORY
-    pre = lib.fa_bwd_preprocess(*([0x10000] * 5 + [0]), 1, 1, 16, 64, None)
+    pre = lib.fa_bwd_preprocess(*([0x10000] * 4 + [0]), 1, 1, 16, 64, None)
     assert pre == fa.FA_ERR_INVALID_ARG
+    dq = lib.fa_bwd_dq(*([0x10000] * 7), 1, 1, 16, 64, 1, 0.0, None)
+    assert dq == fa.FA_ERR_INVALID_ARG
+    dq = lib.fa_bwd_dq(*([0x10000] * 6 + [0x10008]), 1, 1, 16, 64, 1, 0.125, None)
+    assert dq == fa.FA_ERR_MISALIGNED
 
 
 def test_binding_rejects_cpu_tensors(fa):

@@ -254,3 +254,18 @@ def test_workspace_path_matches_library_allocation(fa, dev):
     b = fa.attention_bwd(q, k, v, o, do, lse, causal=True, scale=s)
     for ga, gb in zip(a, b):
         assert float((ga - gb).abs().max()) <= 1e-5
+
+
+def test_backward_is_deterministic(fa, dev):
+    """Every gradient entry is one sum in a fixed order: repeated calls agree bit for bit."""
+    import torch
+    B, H, N, d = 2, 4, 1000, 128
+    x = inputs(10, B, H, N, d)
+    s = scale_for(d)
+    q, k, v, do = (to_device_bf16(x[n + "_bits"], dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, causal=True, scale=s)
+    a = fa.attention_bwd(q, k, v, o, do, lse, causal=True, scale=s)
+    b = fa.attention_bwd(q, k, v, o, do, lse, causal=True, scale=s)
+    torch.cuda.synchronize()
+    for ga, gb in zip(a, b):
+        assert torch.equal(ga, gb)

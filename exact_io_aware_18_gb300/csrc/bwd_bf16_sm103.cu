@@ -36,7 +36,8 @@
 //               own 64 S^T columns.  Phase dS: dS^T = P o (dP^T - D), BF16,
 //               likewise into its own dP^T columns (scale is applied to dK
 //               once, when it leaves TMEM).  At the end: dK, dV rows out of
-//               TMEM to global memory (FP32).
+//               TMEM into swizzled shared-memory boxes, then to global memory
+//               (FP32) by TMA stores of whole 128-byte rows.
 // TMEM columns: S^T [0,128) (P^T halves at [0,32) and [64,96)),
 // dP^T [128,256) (dS^T halves at [128,160) and [192,224)), dV [256,256+d),
 // dK [256+d, 256+2d).  Eleven warps cap a thread at 168 registers (the
@@ -69,6 +70,10 @@ struct BwdCfg {
     static constexpr int SMEM_BYTES =
         (LAYOUT_BYTES + 1024 <= kMaxDynSmem) ? LAYOUT_BYTES + 1024 : kMaxDynSmem;
     static_assert(LAYOUT_BYTES <= kMaxDynSmem, "backward tiles do not fit in shared memory");
+    // The epilogue stages FP32 dV and dK (2 x 8 warps x d/64 boxes of 4 KB)
+    // over K, V and the stage ring, which start at offset 0 and are contiguous.
+    static_assert(OFF_K == 0 && 2 * 8 * (D / 64) * 4096 <= OFF_VEC,
+                  "dK/dV staging does not fit over the tiles");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
     static constexpr int THREADS = 352;
@@ -95,8 +100,10 @@ __global__ void __launch_bounds__(352, 1)
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dk,
+                         const __grid_constant__ CUtensorMap tm_dv,
                          const float* __restrict__ delta, const float* __restrict__ lse2,
-                         float* __restrict__ dk, float* __restrict__ dv, int N, int n_pad,
+                         int N, int n_pad,
                          int BH, int n_tiles, int group, float scale, float scale_log2,
                          unsigned int* status, unsigned long long timeout_ns) {
     using C = BwdCfg<D>;
@@ -163,7 +170,6 @@ __global__ void __launch_bounds__(352, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const WaitCtx wc{status, timeout_ns, abort_flag};
-    const long long head_row0 = static_cast<long long>(bh) * N;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -329,28 +335,35 @@ __global__ void __launch_bounds__(352, 1)
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::ACC_FULL), 0, wc));
         if (ok) {
+            // Every MMA has completed, so K, V and the [Q | dO] ring hold the
+            // staging boxes: this warp's 32 rows x d/2 columns of dV, then of
+            // dK, as d/64 boxes of 32 x 32 each, stored by TMA in whole
+            // 128-byte rows.
             tc_fence_after();
-            float4* dv_row = reinterpret_cast<float4*>(dv + (head_row0 + kglob) * D + (D / 2) * h);
-            float4* dk_row = reinterpret_cast<float4*>(dk + (head_row0 + kglob) * D + (D / 2) * h);
+            constexpr uint32_t kHalfBytes = 8 * (D / 64) * 4096;  // all of dV
+            const uint32_t stg = s_k + static_cast<uint32_t>((warp - 2) * (D / 64) * 4096);
 #pragma unroll
             for (int ch = 0; ch < D / 64; ++ch) {
-                uint32_t a[32], b[32];
+                uint32_t a[32];
                 tmem_ld32(t_lane + C::COL_DV + (D / 2) * h + ch * 32, a);
-                tmem_ld32(t_lane + C::COL_DK + (D / 2) * h + ch * 32, b);
-                if (!key_pad) {
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        dv_row[ch * 8 + u] =
-                            make_float4(__uint_as_float(a[4 * u]), __uint_as_float(a[4 * u + 1]),
-                                        __uint_as_float(a[4 * u + 2]),
-                                        __uint_as_float(a[4 * u + 3]));
-                        dk_row[ch * 8 + u] = make_float4(
-                            __uint_as_float(b[4 * u]) * scale, __uint_as_float(b[4 * u + 1]) * scale,
-                            __uint_as_float(b[4 * u + 2]) * scale,
-                            __uint_as_float(b[4 * u + 3]) * scale);
-                    }
-                }
+                st_row_sw128_f32(stg + ch * 4096, lane, a, 1.f);
+                tmem_ld32(t_lane + C::COL_DK + (D / 2) * h + ch * 32, a);
+                st_row_sw128_f32(stg + kHalfBytes + ch * 4096, lane, a, scale);
             }
+            fence_async_smem();
+            __syncwarp();
+            const int row0 = kt * C::BN + wq * 32;
+            if (lane == 0 && row0 < N) {
+#pragma unroll
+                for (int ch = 0; ch < D / 64; ++ch) {
+                    tma_store_3d(&tm_dv, stg + ch * 4096, (D / 2) * h + ch * 32, row0, bh);
+                    tma_store_3d(&tm_dk, stg + kHalfBytes + ch * 4096, (D / 2) * h + ch * 32,
+                                 row0, bh);
+                }
+                bulk_commit();
+                bulk_wait_read_all();  // the boxes stay in place until read
+            }
+            __syncwarp();
         }
     }
 
@@ -381,7 +394,7 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     if (group < 1) group = 1;
     dim3 grid(n_tiles, a.H, a.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, a.delta, a.lse2, a.dk, a.dv, a.N, a.n_pad,
+        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dk, *a.tm_dv, a.delta, a.lse2, a.N, a.n_pad,
         a.B * a.H, n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
     return cudaGetLastError();
 }

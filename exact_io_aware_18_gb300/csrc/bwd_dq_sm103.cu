@@ -30,7 +30,8 @@
 //               P' = exp2(S * scale*log2e - LSE2_r + log2 scale) = scale P,
 //               dS' = P' o (dP - D_r) = scale dS, BF16, written over the first
 //               32 of its own 64 S columns.  At the end: the dQ row half out
-//               of TMEM to global memory (FP32).
+//               of TMEM into swizzled shared-memory boxes, then to global
+//               memory (FP32) by TMA stores of whole 128-byte rows.
 // TMEM columns: S buffers [0,128) and [128,256), dP [256,384), dQ [384,384+d).
 // All waits are bounded (see sm103_primitives.cuh).
 #include "fa_internal.h"
@@ -60,6 +61,9 @@ struct DqCfg {
     static constexpr int SMEM_BYTES =
         (LAYOUT_BYTES + 1024 <= kMaxDynSmem) ? LAYOUT_BYTES + 1024 : kMaxDynSmem;
     static_assert(LAYOUT_BYTES <= kMaxDynSmem, "dQ tiles do not fit in shared memory");
+    // The epilogue stages the FP32 dQ tile (8 warps x d/64 boxes of 4 KB) over Q and dO.
+    static_assert(8 * (D / 64) * 4096 <= 2 * TILE_BYTES && OFF_DO == OFF_Q + TILE_BYTES,
+                  "dQ staging does not fit over Q and dO");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_DP = 256, COL_DQ = 384;
     static constexpr int THREADS = 352;
@@ -88,8 +92,8 @@ __global__ void __launch_bounds__(352, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do,
-                       const float* __restrict__ delta, const float* __restrict__ lse2,
-                       float* __restrict__ dq, int N, int n_pad, int BH, int n_tiles, int group,
+                       const __grid_constant__ CUtensorMap tm_dq,
+                       const float* __restrict__ delta, const float* __restrict__ lse2, int N, int n_pad, int BH, int n_tiles, int group,
                        float scale, float scale_log2, unsigned int* status,
                        unsigned long long timeout_ns) {
     using C = DqCfg<D>;
@@ -318,22 +322,29 @@ __global__ void __launch_bounds__(352, 1)
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DQ_DONE), 0, wc));
         if (ok) {
+            // Every MMA has completed, so Q and dO (512 d bytes, the size of
+            // the FP32 dQ tile) hold the staging boxes: this warp's 32 rows x
+            // d/2 columns as d/64 boxes of 32 x 32, stored by TMA in whole
+            // 128-byte rows.
             tc_fence_after();
-            float4* dq_row = reinterpret_cast<float4*>(
-                dq + (static_cast<long long>(bh) * N + qglob) * D + (D / 2) * h);
+            const uint32_t stg = s_q + static_cast<uint32_t>((warp - 2) * (D / 64) * 4096);
 #pragma unroll
             for (int ch = 0; ch < D / 64; ++ch) {
                 uint32_t a[32];
                 tmem_ld32(t_lane + C::COL_DQ + (D / 2) * h + ch * 32, a);
-                if (qglob < N) {
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        dq_row[ch * 8 + u] =
-                            make_float4(__uint_as_float(a[4 * u]), __uint_as_float(a[4 * u + 1]),
-                                        __uint_as_float(a[4 * u + 2]),
-                                        __uint_as_float(a[4 * u + 3]));
-                }
+                st_row_sw128_f32(stg + ch * 4096, lane, a, 1.f);
             }
+            fence_async_smem();
+            __syncwarp();
+            const int row0 = qt * C::BM + wq * 32;
+            if (lane == 0 && row0 < N) {
+#pragma unroll
+                for (int ch = 0; ch < D / 64; ++ch)
+                    tma_store_3d(&tm_dq, stg + ch * 4096, (D / 2) * h + ch * 32, row0, bh);
+                bulk_commit();
+                bulk_wait_read_all();  // the boxes stay in place until read
+            }
+            __syncwarp();
         }
     }
 
@@ -363,7 +374,7 @@ cudaError_t launch_t(const DqArgs& a, cudaStream_t stream) {
     if (group < 1) group = 1;
     dim3 grid(n_tiles, a.H, a.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, a.delta, a.lse2, a.dq, a.N, a.n_pad, a.B * a.H,
+        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, a.delta, a.lse2, a.N, a.n_pad, a.B * a.H,
         n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
     return cudaGetLastError();
 }

@@ -78,6 +78,23 @@ int make_map_bf16(CUtensorMap* map, const void* ptr, int d, int N, long long BH)
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// FP32 gradient (d, N, B*H) written by TMA stores: 32 x 32 boxes (128-byte
+// rows), 128-byte swizzle.  Rows past N are clipped by the copy engine.
+int make_map_f32_out(CUtensorMap* map, float* ptr, int d, int N, long long BH) {
+    EncodeFn enc;
+    if (int rc = get_encode(&enc)) return rc;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(int B, int H, int N, int d, float scale) {
@@ -177,12 +194,14 @@ int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
     unsigned int* status;
     if (int rc = status_ptr(&status)) return rc;
     const long long BH = static_cast<long long>(B) * H;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
     if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
-    fa::BwdArgs a{&tq, &tk, &tv, &tdo, delta_ws, lse2_ws, dk, dv, B, H, N, d,
+    if (int rc = make_map_f32_out(&tdk, dk, d, N, BH)) return rc;
+    if (int rc = make_map_f32_out(&tdv, dv, d, N, BH)) return rc;
+    fa::BwdArgs a{&tq, &tk, &tv, &tdo, &tdk, &tdv, delta_ws, lse2_ws, B, H, N, d,
                   static_cast<int>(n_pad_of(N)), causal ? 1 : 0, scale,
                   scale * 1.4426950408889634f, status, g_timeout_ns.load()};
     return launch_rc(fa::launch_bwd_dkdv_bf16(a, static_cast<cudaStream_t>(stream)));
@@ -196,12 +215,13 @@ int fa_bwd_dq(const void* q, const void* k, const void* v, const void* do_,
     unsigned int* status;
     if (int rc = status_ptr(&status)) return rc;
     const long long BH = static_cast<long long>(B) * H;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
-    fa::DqArgs a{&tq, &tk, &tv, &tdo, delta_ws, lse2_ws, dq, B, H, N, d,
+    if (int rc = make_map_f32_out(&tdq, dq, d, N, BH)) return rc;
+    fa::DqArgs a{&tq, &tk, &tv, &tdo, &tdq, delta_ws, lse2_ws, B, H, N, d,
                  static_cast<int>(n_pad_of(N)), causal ? 1 : 0, scale,
                  scale * 1.4426950408889634f, status, g_timeout_ns.load()};
     return launch_rc(fa::launch_bwd_dq_bf16(a, static_cast<cudaStream_t>(stream)));

@@ -39,16 +39,17 @@ struct BwdPreArgs {
 
 cudaError_t launch_bwd_pre_bf16(const BwdPreArgs& a, cudaStream_t stream);
 
-// Backward dK/dV (BF16).  Tensor maps for Q, K, V, dO as for the forward.
+// Backward dK/dV (BF16).  Tensor maps for Q, K, V, dO as for the forward;
+// dK and dV through FP32 maps (d, N, B*H) with 32 x 32 boxes, 128-byte swizzle.
 struct BwdArgs {
     const CUtensorMap* tm_q;
     const CUtensorMap* tm_k;
     const CUtensorMap* tm_v;
     const CUtensorMap* tm_do;
+    const CUtensorMap* tm_dk;
+    const CUtensorMap* tm_dv;
     const float* delta;
     const float* lse2;
-    float* dk;
-    float* dv;
     int B, H, N, d, n_pad;
     int causal;
     float scale;       // multiplies dS (dQ = dS K, dK = dS^T Q with dS scaled)
@@ -59,15 +60,16 @@ struct BwdArgs {
 
 cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t stream);
 
-// Backward dQ (BF16): one CTA per Q tile, loop over key tiles, dq written once.
+// Backward dQ (BF16): one CTA per Q tile, loop over key tiles, dq written
+// once through an FP32 map like dK's.
 struct DqArgs {
     const CUtensorMap* tm_q;
     const CUtensorMap* tm_k;
     const CUtensorMap* tm_v;
     const CUtensorMap* tm_do;
+    const CUtensorMap* tm_dq;
     const float* delta;
     const float* lse2;
-    float* dq;
     int B, H, N, d, n_pad;
     int causal;
     float scale;

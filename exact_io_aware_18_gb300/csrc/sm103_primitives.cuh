@@ -158,6 +158,29 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA stores, tcgen05.mma operand reads).
+// Stores four 32-bit words at a 16-byte aligned shared address.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Writes 32 FP32 words (one 128-byte row) as row `row` of a box that a TMA
+// store with 128-byte swizzle reads: 16-byte chunk c lands at chunk c ^ (row & 7).
+// `box` is 1024-byte aligned.  Eight consecutive rows hit distinct banks.
+__device__ __forceinline__ void st_row_sw128_f32(uint32_t box, int row, const uint32_t (&w)[32],
+                                                 float mul) {
+    const uint32_t base = box + static_cast<uint32_t>(row) * 128u;
+    const uint32_t x = static_cast<uint32_t>(row & 7);
+#pragma unroll
+    for (uint32_t c = 0; c < 8; ++c)
+        st_shared_v4(base + ((c ^ x) << 4), __float_as_uint(__uint_as_float(w[4 * c]) * mul),
+                     __float_as_uint(__uint_as_float(w[4 * c + 1]) * mul),
+                     __float_as_uint(__uint_as_float(w[4 * c + 2]) * mul),
+                     __float_as_uint(__uint_as_float(w[4 * c + 3]) * mul));
+}
+
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -11,20 +11,25 @@
 // the division by l deferred to the end ("FlashAttention-2", technical
 // architecture, improvement 1).
 //
-// GB300 mapping (one CTA per SM, 192 threads):
+// GB300 mapping (one CTA per SM, 320 threads):
 //   warp 0      TMA producer: Q tile once, then K_j and V_j into an NS-deep
 //               shared-memory ring (128-byte swizzle, 64-column boxes).
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
 //               score buffers, then O += P_{j-1} V_{j-1} with P read straight
 //               from TMEM, so the tensor core works on S_{j+1} while the
 //               softmax warps work on S_j.
-//   warps 2..5  softmax: thread r owns query row r (TMEM lane r): loads its
-//               row of S, masks, updates m and l, writes P as BF16 over the
-//               first half of the same TMEM columns, and rescales the O
-//               accumulator only when its max grew by more than 2^8 (the
-//               final O / l and LSE use the same stale max, so the result is
-//               unchanged).  Epilogue: O / l to BF16 through shared memory and
-//               a TMA store; LSE = ln 2 * (m + log2 l).
+//   warps 2..9  softmax: thread (r, h) owns query row r (TMEM lane r) and
+//               keys [64h, 64h+64) of every tile (warps 2-5: h = 0, 6-9:
+//               h = 1), so two warps share each SM sub-partition's rows and
+//               hide each other's latency.  Per tile: load its 64 scores,
+//               mask, swap the partial row max with the partner warp through
+//               shared memory, update m and its half of l, write P as BF16
+//               over the first 32 of its own 64 S columns, and rescale its
+//               d/2 columns of the O accumulator only when the max grew by
+//               more than 2^8 (the final O / l and LSE use the same stale
+//               max, so the result is unchanged).  Epilogue: the two halves of
+//               l are summed, O / l goes to BF16 through shared memory and a
+//               TMA store; LSE = ln 2 * (m + log2 l).
 //
 // TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+d).  All waits are
 // bounded (see sm103_primitives.cuh).
@@ -47,10 +52,12 @@ struct FwdCfg {
     static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
     static constexpr int BAR_BYTES = 512;
-    static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+    static constexpr int OFF_XCH = OFF_BAR + BAR_BYTES;  // row maxima and sums of the halves
+    static constexpr int XCH_BYTES = 6 * 128 * 4;
+    static constexpr int SMEM_BYTES = OFF_XCH + XCH_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 320;
 };
 
 // Barrier slots (8 bytes each) inside the barrier area.
@@ -69,7 +76,7 @@ struct FwdBars {
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
@@ -112,7 +119,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(Bar::S_FULL + b), 1);
-            mbar_init(bar(Bar::P_FULL + b), 4);
+            mbar_init(bar(Bar::P_FULL + b), 8);  // one arrival per softmax warp
         }
         mbar_init(bar(Bar::O_FULL), 1);
         mbar_init(bar(Bar::DONE), 1);
@@ -187,7 +194,9 @@ __global__ void __launch_bounds__(192, 1)
                 for (int kk = 0; kk < C::BN / 16; ++kk) {
                     // V as an MN-major B operand: 16 keys = 2 atoms of 8 rows.
                     const uint64_t bd = smem_desc_sw128(v_tile + kk * 2048, C::BOX_BYTES, 1024);
-                    mma_ts(tmem + C::COL_O, a_tmem + kk * 8, bd, id_pv, (t > 0 || kk > 0));
+                    // P halves (keys 0-63, 64-127) sit at columns [0,32) and [64,96).
+                    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                    mma_ts(tmem + C::COL_O, a_tmem + acol, bd, id_pv, (t > 0 || kk > 0));
                 }
                 tc_commit(bar(Bar::V_EMPTY + st));
                 tc_commit(bar(Bar::O_FULL));
@@ -218,39 +227,53 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
+        // Thread (row, h): query row `row` (TMEM lane), keys [64h, 64h+64) of
+        // each tile and O columns [h d/2, (h+1) d/2).  The two warps that share
+        // a lane quarter swap their partial row maxima through shared memory
+        // once per tile, so both apply the same running max.
         const int wq = warp & 3;             // TMEM lane quarter of this warp
+        const int h = (warp - 2) >> 2;       // key / O-column half
         const int row = wq * 32 + lane;      // row inside the Q tile
         const int grow = qt * C::BM + row;   // query index inside the head
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const uint32_t pair_bar = 1 + wq;    // named barrier of the two warps
+        float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);  // [2][2][128] maxima, [2][128] sums
         float m_run = -INFINITY;  // running max, base-2 units of scale * S
-        float l_run = 0.f;        // running sum of 2^(x - m_run)
+        float l_run = 0.f;        // this half's running sum of 2^(x - m_run)
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const int b = j & 1;
-            const uint32_t t_s = t_lane + (b ? C::COL_S1 : C::COL_S0);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_FULL + b), (j >> 1) & 1, wc));
-            if (!ok) break;
-            tc_fence_after();
-            float s[128];
+            const uint32_t t_s = t_lane + (b ? C::COL_S1 : C::COL_S0) + 64 * h;
+            // A failed wait is carried to the pair barrier rather than breaking
+            // here, so that both warps leave the loop at the same barrier.
+            bool okw = ok && __all_sync(0xffffffffu,
+                                        mbar_wait(bar(Bar::S_FULL + b), (j >> 1) & 1, wc));
+            float s[64];
+            float mx = -INFINITY;
+            if (okw) {
+                tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(t_s + c * 32, r);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_s + c * 32, r);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
-            }
-            const int key0 = j * C::BN;
-            if ((CAUSAL && j == qt) || key0 + C::BN > N) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int key = key0 + c;
-                    if ((CAUSAL && key > grow) || key >= N) s[c] = -INFINITY;
+                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
                 }
-            }
-            float mx = s[0];
+                const int key0 = j * C::BN + 64 * h;  // key index of entry 0
+                if ((CAUSAL && j == qt) || key0 + 64 > N) {
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-            const float m_tile = mx * scale_log2;
+                    for (int c = 0; c < 64; ++c) {
+                        const int key = key0 + c;
+                        if ((CAUSAL && key > grow) || key >= N) s[c] = -INFINITY;
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
+            }
+            xch[(b * 2 + h) * 128 + row] = mx;
+            ok = named_bar_and(pair_bar, 64, okw);
+            if (!ok) break;
+            const float m_tile = fmaxf(mx, xch[(b * 2 + (h ^ 1)) * 128 + row]) * scale_log2;
             const bool rescale = m_tile > m_run + 8.0f;
             float alpha = 1.f;
             if (rescale) {
@@ -259,35 +282,34 @@ __global__ void __launch_bounds__(192, 1)
             }
             const float neg_m = -m_run;
             float sum = 0.f;
+            uint32_t pk[32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * e], scale_log2, neg_m));
-                    const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * e + 1], scale_log2, neg_m));
-                    sum += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(t_s + h * 32, pk);
+            for (int e = 0; e < 32; ++e) {
+                const float p0 = ex2_approx(fmaf(s[2 * e], scale_log2, neg_m));
+                const float p1 = ex2_approx(fmaf(s[2 * e + 1], scale_log2, neg_m));
+                sum += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
             }
+            // P (BF16) over the first 32 of this half's own 64 S columns.
+            tmem_st32(t_s, pk);
             l_run = l_run * alpha + sum;
             tmem_st_wait();
             if (j > 0) {
-                // O holds the sum up to PV_{j-1}; it must be complete before a rescale
-                // and before P_j is released.
+                // O holds the sum up to PV_{j-1}; it must be complete before a
+                // rescale and before P_j is released.
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::O_FULL), (j - 1) & 1, wc));
-                if (!ok) break;
+                if (!ok) continue;  // the next pair barrier (or the loop end) reports it
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < D / 64; ++c) {
                         uint32_t r[32];
-                        tmem_ld32(t_lane + C::COL_O + c * 32, r);
+                        const uint32_t t_o = t_lane + C::COL_O + (D / 2) * h + c * 32;
+                        tmem_ld32(t_o, r);
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        tmem_st32(t_lane + C::COL_O + c * 32, r);
+                        tmem_st32(t_o, r);
                     }
                     tmem_st_wait();
                 }
@@ -296,16 +318,23 @@ __global__ void __launch_bounds__(192, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(Bar::P_FULL + b));
         }
+        // Both warps of the pair reach this barrier after the same iteration.
+        xch[512 + h * 128 + row] = l_run;
+        ok = named_bar_and(pair_bar, 64, ok);
+        const float l_tot = l_run + xch[512 + (h ^ 1) * 128 + row];
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::O_FULL), (n_kv - 1) & 1, wc));
         if (ok) {
             tc_fence_after();
-            const float inv_l = 1.f / l_run;
-            if (grow < N) lse[static_cast<long long>(bh) * N + grow] =
-                              (m_run + lg2_approx(l_run)) * 0.69314718055994531f;
-            // O / l -> bf16 into the (now free) Q buffer, in the TMA box layout.
+            const float inv_l = 1.f / l_tot;
+            if (h == 0 && grow < N)
+                lse[static_cast<long long>(bh) * N + grow] =
+                    (m_run + lg2_approx(l_tot)) * 0.69314718055994531f;
+            // O / l -> bf16 into the (now free) Q buffer, in the TMA box layout:
+            // this half's d/2 columns are 32-column chunks h d/64 ... .
             uint8_t* stage = smem + C::OFF_Q;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 64; ++cc) {
+                const int c = h * (D / 64) + cc;  // 32-column chunk of the row
                 uint32_t r[32];
                 tmem_ld32(t_lane + C::COL_O + c * 32, r);
                 const int box = c >> 1;
@@ -327,12 +356,12 @@ __global__ void __launch_bounds__(192, 1)
             }
             fence_async_smem();
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(5, 256);
         if (ok && threadIdx.x == 64 && !*abort_flag) {
             for (int kb = 0; kb < C::KB; ++kb)
                 tma_store_3d(&tm_o, s_q + kb * C::BOX_BYTES, kb * 64, qt * C::BM, bh);
             bulk_commit();
-            bulk_wait_all();
+            bulk_wait_read_all();  // the Q buffer stays in place until read
         }
     }
 

@@ -11,27 +11,33 @@
 // the division by l deferred to the end ("FlashAttention-2", technical
 // architecture, improvement 1).
 //
-// GB300 mapping (one CTA per SM, 320 threads):
+// GB300 mapping (one CTA per SM, 352 threads):
 //   warp 0      TMA producer: Q tile once, then K_j and V_j into an NS-deep
 //               shared-memory ring (128-byte swizzle, 64-column boxes).
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//               score buffers, then O += P_{j-1} V_{j-1} with P read straight
-//               from TMEM, so the tensor core works on S_{j+1} while the
-//               softmax warps work on S_j.
+//   warps 1, 10 two MMA issuers (one thread each).  A: S_j = Q K_j^T into one
+//               of two TMEM score buffers, once the softmax warps have read
+//               S_{j-2} out of it.  B: O += P_j V_j as soon as the softmax
+//               warps release P_j.  Both take A from TMEM (Q, copied there
+//               once, and P), so consecutive MMAs never switch the A source,
+//               which drains the tensor pipe.  One thread issues MMAs no
+//               faster than the pipe runs them, so two issuers keep it fed
+//               while either waits.
 //   warps 2..9  softmax: thread (r, h) owns query row r (TMEM lane r) and
 //               keys [64h, 64h+64) of every tile (warps 2-5: h = 0, 6-9:
 //               h = 1), so two warps share each SM sub-partition's rows and
-//               hide each other's latency.  Per tile: load its 64 scores,
-//               mask, swap the partial row max with the partner warp through
-//               shared memory, update m and its half of l, write P as BF16
-//               over the first 32 of its own 64 S columns, and rescale its
+//               hide each other's latency.  First, Q row half into TMEM.  Per
+//               tile: load its 64 scores (then the S buffer is free), mask,
+//               swap the partial row max with the partner warp through shared
+//               memory, update m and its half of l, write P as BF16 into the
+//               P buffer once PV_{j-1} has read it, and rescale its
 //               d/2 columns of the O accumulator only when the max grew by
 //               more than 2^8 (the final O / l and LSE use the same stale
 //               max, so the result is unchanged).  Epilogue: the two halves of
 //               l are summed, O / l goes to BF16 through shared memory and a
 //               TMA store; LSE = ln 2 * (m + log2 l).
 //
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+d).  All waits are
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+d), Q [256+d, 256+3d/2),
+// P [256+3d/2, 320+3d/2) (all 512 columns at d = 128).  All waits are
 // bounded (see sm103_primitives.cuh).
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
@@ -56,8 +62,12 @@ struct FwdCfg {
     static constexpr int XCH_BYTES = 6 * 128 * 4;
     static constexpr int SMEM_BYTES = OFF_XCH + XCH_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
+    // S0, S1: scores (FP32); O: accumulator (FP32); Q and P: BF16 pairs, the
+    // A operands of S = Q K^T and O += P V.
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
-    static constexpr int THREADS = 320;
+    static constexpr uint32_t COL_Q = COL_O + D, COL_P = COL_Q + D / 2;
+    static_assert(COL_P + BN / 2 <= TMEM_COLS, "TMEM columns");
+    static constexpr int THREADS = 352;
 };
 
 // Barrier slots (8 bytes each) inside the barrier area.
@@ -69,14 +79,16 @@ struct FwdBars {
     static constexpr int K_EMPTY = V_FULL + NS;
     static constexpr int V_EMPTY = K_EMPTY + NS;
     static constexpr int S_FULL = V_EMPTY + NS;  // 2
-    static constexpr int P_FULL = S_FULL + 2;    // 2
-    static constexpr int O_FULL = P_FULL + 2;
+    static constexpr int S_EMPTY = S_FULL + 2;   // 2
+    static constexpr int QT_FULL = S_EMPTY + 2;
+    static constexpr int P_FULL = QT_FULL + 1;
+    static constexpr int O_FULL = P_FULL + 1;
     static constexpr int DONE = O_FULL + 1;
     static constexpr int COUNT = DONE + 1;
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
@@ -119,10 +131,12 @@ __global__ void __launch_bounds__(320, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(Bar::S_FULL + b), 1);
-            mbar_init(bar(Bar::P_FULL + b), 8);  // one arrival per softmax warp
+            mbar_init(bar(Bar::S_EMPTY + b), 8);  // one arrival per softmax warp
         }
+        mbar_init(bar(Bar::QT_FULL), 8);
+        mbar_init(bar(Bar::P_FULL), 8);
         mbar_init(bar(Bar::O_FULL), 1);
-        mbar_init(bar(Bar::DONE), 1);
+        mbar_init(bar(Bar::DONE), 2);  // one commit per issuer
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tensormap(&tm_q);
@@ -177,52 +191,59 @@ __global__ void __launch_bounds__(320, 1)
                 mbar_wait_drain(bar(Bar::V_FULL + j % C::NS), (j / C::NS) & 1, timeout_ns);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 10) {
+        // ------------------------------------------------------------ MMA issuers
+        // Every MMA takes its A operand from TMEM: a 128 x 128 x 16 MMA that
+        // follows one with A in shared memory (or the reverse) waits for the
+        // pipe to drain, which cost about a third of the tensor time.
         if (lane == 0) {
-            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
-            constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);
-            auto issue_pv = [&](int t) -> bool {
-                const int b = t & 1;
-                const int st = t % C::NS;
-                if (!mbar_wait(bar(Bar::P_FULL + b), (t >> 1) & 1, wc)) return false;
-                if (!mbar_wait(bar(Bar::V_FULL + st), (t / C::NS) & 1, wc)) return false;
-                tc_fence_after();
-                const uint32_t a_tmem = tmem + (b ? C::COL_S1 : C::COL_S0);
-                const uint32_t v_tile = s_v + st * C::TILE_BYTES;
+            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // B = K, K-major
+            constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);   // B = V, MN-major
+            if (warp == 10) {
+                // Issuer B: O += P_t V_t as soon as the softmax warps release P_t.
+                bool ok = true;
+                for (int t = 0; t < n_kv && ok; ++t) {
+                    const int st = t % C::NS;
+                    ok = mbar_wait(bar(Bar::P_FULL), t & 1, wc) &&
+                         mbar_wait(bar(Bar::V_FULL + st), (t / C::NS) & 1, wc);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t v_tile = s_v + st * C::TILE_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk) {
-                    // V as an MN-major B operand: 16 keys = 2 atoms of 8 rows.
-                    const uint64_t bd = smem_desc_sw128(v_tile + kk * 2048, C::BOX_BYTES, 1024);
-                    // P halves (keys 0-63, 64-127) sit at columns [0,32) and [64,96).
-                    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-                    mma_ts(tmem + C::COL_O, a_tmem + acol, bd, id_pv, (t > 0 || kk > 0));
+                    for (int kk = 0; kk < C::BN / 16; ++kk) {
+                        // V as an MN-major B operand: 16 keys = 2 atoms of 8 rows.
+                        const uint64_t bd =
+                            smem_desc_sw128(v_tile + kk * 2048, C::BOX_BYTES, 1024);
+                        mma_ts(tmem + C::COL_O, tmem + C::COL_P + kk * 8, bd, id_pv,
+                               (t > 0 || kk > 0));
+                    }
+                    tc_commit(bar(Bar::V_EMPTY + st));
+                    tc_commit(bar(Bar::O_FULL));
                 }
-                tc_commit(bar(Bar::V_EMPTY + st));
-                tc_commit(bar(Bar::O_FULL));
-                return true;
-            };
-            bool ok = mbar_wait(bar(Bar::Q_FULL), 0, wc);
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j % C::NS;
-                const int b = j & 1;
-                ok = mbar_wait(bar(Bar::K_FULL + st), (j / C::NS) & 1, wc);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t k_tile = s_k + st * C::TILE_BYTES;
-                const uint32_t d_tmem = tmem + (b ? C::COL_S1 : C::COL_S0);
+            } else {
+                // Issuer A: S_j = Q K_j^T into buffer j & 1 once the softmax
+                // warps have read S_{j-2} out of it.  The next phase of that
+                // buffer's S_EMPTY needs S_j itself, so the wait cannot miss it.
+                bool ok = mbar_wait(bar(Bar::QT_FULL), 0, wc);
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    const int st = j % C::NS;
+                    const int b = j & 1;
+                    if (j >= 2) ok = mbar_wait(bar(Bar::S_EMPTY + b), ((j - 2) >> 1) & 1, wc);
+                    ok = ok && mbar_wait(bar(Bar::K_FULL + st), (j / C::NS) & 1, wc);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t k_tile = s_k + st * C::TILE_BYTES;
+                    const uint32_t d_tmem = tmem + (b ? C::COL_S1 : C::COL_S0);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                    const uint64_t ad = smem_desc_sw128(s_q + koff, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(k_tile + koff, 16, 1024);
-                    mma_ss(d_tmem, ad, bd, id_s, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                        mma_ts(d_tmem, tmem + C::COL_Q + kk * 8,
+                               smem_desc_sw128(k_tile + koff, 16, 1024), id_s, kk > 0);
+                    }
+                    tc_commit(bar(Bar::S_FULL + b));
+                    tc_commit(bar(Bar::K_EMPTY + st));
                 }
-                tc_commit(bar(Bar::S_FULL + b));
-                tc_commit(bar(Bar::K_EMPTY + st));
-                if (j > 0) ok = issue_pv(j - 1);
             }
-            if (ok) issue_pv(n_kv - 1);
         }
         __syncwarp();
     } else {
@@ -240,7 +261,29 @@ __global__ void __launch_bounds__(320, 1)
         float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);  // [2][2][128] maxima, [2][128] sums
         float m_run = -INFINITY;  // running max, base-2 units of scale * S
         float l_run = 0.f;        // this half's running sum of 2^(x - m_run)
-        bool ok = true;
+        // Q into TMEM as BF16 pairs (the A operand of S = Q K^T): this thread's
+        // row, elements [h d/2, (h+1) d/2), read from the swizzled tile.
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::Q_FULL), 0, wc));
+        if (ok) {
+            uint32_t w[D / 4];
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+                const int gc = h * (D / 16) + c;  // 16-byte chunk of the row
+                const uint4 v = *reinterpret_cast<const uint4*>(
+                    smem + C::OFF_Q + (gc >> 3) * C::BOX_BYTES + row * 128 +
+                    (((gc & 7) ^ (row & 7)) << 4));
+                w[4 * c] = v.x;
+                w[4 * c + 1] = v.y;
+                w[4 * c + 2] = v.z;
+                w[4 * c + 3] = v.w;
+            }
+            if constexpr (D == 128) tmem_st32(t_lane + C::COL_Q + h * (D / 4), w);
+            else tmem_st16(t_lane + C::COL_Q + h * (D / 4), w);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Bar::QT_FULL));
+        }
         for (int j = 0; j < n_kv; ++j) {
             const int b = j & 1;
             const uint32_t t_s = t_lane + (b ? C::COL_S1 : C::COL_S0) + 64 * h;
@@ -259,6 +302,10 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
                 }
+                // S_j is in registers: its buffer may take S_{j+2}.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(Bar::S_EMPTY + b));
                 const int key0 = j * C::BN + 64 * h;  // key index of entry 0
                 if ((CAUSAL && j == qt) || key0 + 64 > N) {
 #pragma unroll
@@ -290,33 +337,32 @@ __global__ void __launch_bounds__(320, 1)
                 sum += p0 + p1;
                 pk[e] = pack_bf16x2(p0, p1);
             }
-            // P (BF16) over the first 32 of this half's own 64 S columns.
-            tmem_st32(t_s, pk);
             l_run = l_run * alpha + sum;
-            tmem_st_wait();
             if (j > 0) {
-                // O holds the sum up to PV_{j-1}; it must be complete before a
-                // rescale and before P_j is released.
+                // PV_{j-1} has finished: the P buffer is free, and O holds the
+                // sum up to PV_{j-1}, as a rescale needs.
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::O_FULL), (j - 1) & 1, wc));
                 if (!ok) continue;  // the next pair barrier (or the loop end) reports it
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
+            }
+            // P_j (BF16): keys [64h, 64h+64) at P columns [32h, 32h+32).
+            tmem_st32(t_lane + C::COL_P + 32 * h, pk);
+            if (__any_sync(0xffffffffu, rescale) && j > 0) {
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        uint32_t r[32];
-                        const uint32_t t_o = t_lane + C::COL_O + (D / 2) * h + c * 32;
-                        tmem_ld32(t_o, r);
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t r[32];
+                    const uint32_t t_o = t_lane + C::COL_O + (D / 2) * h + c * 32;
+                    tmem_ld32(t_o, r);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        tmem_st32(t_o, r);
-                    }
-                    tmem_st_wait();
+                    for (int e = 0; e < 32; ++e)
+                        r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    tmem_st32(t_o, r);
                 }
             }
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Bar::P_FULL + b));
+            if (lane == 0) mbar_arrive(bar(Bar::P_FULL));
         }
         // Both warps of the pair reach this barrier after the same iteration.
         xch[512 + h * 128 + row] = l_run;
@@ -367,9 +413,10 @@ __global__ void __launch_bounds__(320, 1)
 
     // ---------------------------------------------------------------- teardown
     __syncthreads();
+    if (warp == 10 && lane == 0) tc_commit(bar(Bar::DONE));
     if (warp == 1) {
         if (lane == 0) {
-            tc_commit(bar(Bar::DONE));
+            tc_commit(bar(Bar::DONE));  // both issuers' MMAs have completed
             mbar_wait_drain(bar(Bar::DONE), 0, timeout_ns);
         }
         __syncwarp();

@@ -11,12 +11,13 @@
 // written once, so the result does not depend on the order in which CTAs run
 // (no atomics; "FlashAttention-2" stresses a deterministic exact result).
 //
-// Roles (352 threads, one CTA per SM):
-//   warp 0      TMA producers: lane 0 loads Q_i and dO_i once, then K_j into a
-//               three-deep ring (K_j is read until the dQ MMA of tile j);
-//               lane 1 loads V_j into a two-deep ring (read only by dP_j).
+// Roles (384 threads, one CTA per SM):
+//   warp 0      TMA producer: Q_i and dO_i once, then K_j into a three-deep
+//               ring (K_j is read until the dQ MMA of tile j).
+//   warp 11     TMA producer: V_j into a two-deep ring (read only by dP_j).
 //               The two rings free at different times, so each has its own
-//               thread and neither load waits behind the other's slot.
+//               thread, and each thread its own warp: two lanes of one warp
+//               that both spin on barriers share one instruction stream.
 //   warps 1, 10 two MMA issuers (one thread each; one thread alone issues a
 //               128 x 128 x 16 MMA no faster than the pipe runs it, so its
 //               barrier checks would idle the pipe).  Issuer A: S_0, S_1, then
@@ -66,7 +67,7 @@ struct DqCfg {
                   "dQ staging does not fit over Q and dO");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_DP = 256, COL_DQ = 384;
-    static constexpr int THREADS = 352;
+    static constexpr int THREADS = 384;
     static constexpr int COMPUTE_WARPS = 8;
 };
 
@@ -87,7 +88,7 @@ struct DqBars {
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_dq_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -183,7 +184,10 @@ __global__ void __launch_bounds__(352, 1)
             mbar_wait_drain(bar(Bar::QD_FULL), 0, timeout_ns);
             for (int j = (issued > C::NSK ? issued - C::NSK : 0); j < issued; ++j)
                 mbar_wait_drain(bar(Bar::K_FULL + j % C::NSK), (j / C::NSK) & 1, timeout_ns);
-        } else if (lane == 1) {
+        }
+        __syncwarp();
+    } else if (warp == 11) {
+        if (lane == 0) {
             int issued = 0;
             for (; issued < n_kv; ++issued) {
                 const int st = issued % C::NSV, use = issued / C::NSV;

@@ -25,6 +25,16 @@ constexpr int kMaxDevices = 64;
 unsigned int* g_status_ptr[kMaxDevices] = {};
 std::mutex g_mutex;
 
+// Tile counters of the persistent kernels.  Each launch takes the next slot
+// of a ring (two words, the second spare); the CTA that makes the launch's
+// last claim puts the counter back to zero, so launches that overlap on
+// different streams use different slots (up to kWorkSlots in flight).
+constexpr int kWorkSlots = 256;
+__device__ unsigned int g_fa_work[2 * kWorkSlots];
+unsigned int* g_work_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+std::atomic<unsigned int> g_work_next{0};
+
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -41,6 +51,29 @@ int status_ptr(unsigned int** out) {
         g_status_ptr[dev] = static_cast<unsigned int*>(p);
     }
     *out = g_status_ptr[dev];
+    return FA_OK;
+}
+
+// A tile-counter pair for one launch and the SM count of the current device.
+int work_slot(unsigned int** out, int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!g_work_ptr[dev]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_fa_work) != cudaSuccess) return FA_ERR_CUDA;
+            int n = 0;
+            if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                n < 1)
+                return FA_ERR_CUDA;
+            g_work_ptr[dev] = static_cast<unsigned int*>(p);
+            g_num_sms[dev] = n;
+        }
+    }
+    const unsigned int slot = g_work_next.fetch_add(1) % kWorkSlots;
+    *out = g_work_ptr[dev] + 2 * slot;
+    *sms = g_num_sms[dev];
     return FA_OK;
 }
 
@@ -165,8 +198,11 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&to, o, d, N, BH)) return rc;
+    unsigned int* work;
+    int sms;
+    if (int rc = work_slot(&work, &sms)) return rc;
     fa::FwdArgs a{&tq, &tk, &tv, &to, lse, B, H, N, d, causal ? 1 : 0,
-                  scale * 1.4426950408889634f, status, g_timeout_ns.load()};
+                  scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms};
     return launch_rc(fa::launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)));
 }
 

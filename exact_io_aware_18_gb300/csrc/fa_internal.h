@@ -22,6 +22,8 @@ struct FwdArgs {
     float scale_log2;  // scale * log2(e)
     unsigned int* status;
     unsigned long long timeout_ns;
+    unsigned int* work;  // tile counter of this launch, zero between launches
+    int num_sms;         // persistent grid size
 };
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);

@@ -185,6 +185,18 @@ __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Register split between warpgroups: every thread of a warpgroup executes the
+// same one.  The sum over warpgroups of (128 x the new count) must stay within
+// the block's launch allocation, or an increase waits for registers forever.
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Named barrier over `nthreads` threads that also returns the AND of every
 // participant's `pred`.  Orders shared memory like bar.sync.  Warps that pass
 // a flag through it always arrive together, so a failed wait in one of them

@@ -164,3 +164,40 @@ def attention_bwd(q, k, v, do, causal: bool, scale: float, heads=None, o_storage
                               _ptr(dv), _ptr(dvec)),
            "oracle_bwd")
     return dq, dk, dv, dvec
+
+
+def _group_size(hq: int, hkv: int) -> int:
+    if hkv < 1 or hq % hkv:
+        raise ValueError("the number of query heads must be a multiple of the K/V heads")
+    return hq // hkv
+
+
+def attention_fwd_gqa(q, k, v, causal: bool, scale: float):
+    """Grouped-query attention: O [B,Hq,N,d] and LSE [B,Hq,N].
+
+    q is [B,Hq,N,d]; k and v are [B,Hkv,N,d] with Hq = g*Hkv, and query head
+    h attends with K/V head h // g (the multi-query and grouped-query variants
+    of "FlashAttention-2"; Hkv = 1 is multi-query).  By definition this is
+    standard attention per query head, i.e. the MHA definition applied to K
+    and V repeated g times along the head axis.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    g = _group_size(q.shape[1], k.shape[1])
+    return attention_fwd(q, np.repeat(k, g, axis=1), np.repeat(v, g, axis=1), causal, scale)
+
+
+def attention_bwd_gqa(q, k, v, do, causal: bool, scale: float, o_storage="exact"):
+    """dQ [B,Hq,N,d], dK and dV [B,Hkv,N,d], D [B,Hq,N]: the gradient of
+    attention_fwd_gqa.  Repeating K/V along the head axis is linear and its
+    transpose sums over the group, so dK (dV) of K/V head j is the sum of the
+    MHA dK (dV) of the g query heads that read it.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    g = _group_size(Hq, Hkv)
+    dq, dk, dv, dvec = attention_bwd(q, np.repeat(k, g, axis=1), np.repeat(v, g, axis=1), do,
+                                     causal, scale, o_storage=o_storage)
+    dk = dk.reshape(B, Hkv, g, N, d).sum(axis=2)
+    dv = dv.reshape(B, Hkv, g, N, d).sum(axis=2)
+    return dq.reshape(B, Hq, N, d), dk, dv, dvec.reshape(B, Hq, N)

@@ -340,3 +340,71 @@ def test_stored_output_is_exact_when_o_is_representable(oracle_lib):
     b = oracle_lib.attention_bwd(q, k, v, do, False, 0.5, o_storage="bf16")
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+# ---------------------------------------------------------------- grouped-query attention
+
+def _gqa_inputs(seed, B, Hq, Hkv, N, d):
+    q, k, v, do = _rand(seed, B, Hq, N, d)
+    return q, np.ascontiguousarray(k[:, :Hkv]), np.ascontiguousarray(v[:, :Hkv]), do
+
+
+def test_gqa_with_one_query_head_per_group_is_mha(oracle_lib):
+    q, k, v, do = _rand(40, 2, 3, 9, 4)
+    for causal in (False, True):
+        a = oracle_lib.attention_fwd(q, k, v, causal, 0.5)
+        b = oracle_lib.attention_fwd_gqa(q, k, v, causal, 0.5)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b))
+        ga = oracle_lib.attention_bwd(q, k, v, do, causal, 0.5)
+        gb = oracle_lib.attention_bwd_gqa(q, k, v, do, causal, 0.5)
+        for x, y in zip(ga, gb):
+            assert np.array_equal(x.reshape(y.shape), y)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (6, 3), (4, 1)])
+def test_gqa_query_head_reads_its_group(oracle_lib, Hq, Hkv):
+    # query head h attends with K/V head h // (Hq / Hkv), one head at a time
+    B, N, d = 2, 7, 4
+    q, k, v, _ = _gqa_inputs(41, B, Hq, Hkv, N, d)
+    g = Hq // Hkv
+    o, lse = oracle_lib.attention_fwd_gqa(q, k, v, True, 0.5)
+    for b in range(B):
+        for h in range(Hq):
+            j = h // g
+            o1, l1 = oracle_lib.attention_fwd(q[b:b + 1, h:h + 1], k[b:b + 1, j:j + 1],
+                                              v[b:b + 1, j:j + 1], True, 0.5)
+            assert np.array_equal(o[b, h], o1[0, 0]) and np.array_equal(lse[b, h], l1[0, 0])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (3, 1)])
+def test_gqa_backward_matches_finite_differences(oracle_lib, causal, Hq, Hkv):
+    # perturbing one K/V entry moves every query head of its group, so this
+    # pins the group sums of dK and dV as well as dQ
+    N, d, s = 5, 3, 0.6
+    q, k, v, do = (t.astype(np.float64) for t in _gqa_inputs(42 + Hq, 1, Hq, Hkv, N, d))
+
+    def loss(qq, kk, vv):
+        o, _ = oracle_lib.attention_fwd_gqa(qq, kk, vv, causal, s)
+        return float((do * o).sum())
+
+    dq, dk, dv, _ = oracle_lib.attention_bwd_gqa(q, k, v, do, causal, s)
+    h = 1e-6
+    for grad, which in ((dq, 0), (dk, 1), (dv, 2)):
+        base = (q, k, v)[which]
+        num = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            args_p = [q.copy(), k.copy(), v.copy()]
+            args_m = [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += h
+            args_m[which][idx] -= h
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        scale_ref = max(1.0, np.max(np.abs(num)))
+        assert np.max(np.abs(grad - num)) <= 1e-6 * scale_ref, which
+
+
+def test_gqa_rejects_heads_that_do_not_divide(oracle_lib):
+    q = np.zeros((1, 3, 4, 2))
+    k = np.zeros((1, 2, 4, 2))
+    with pytest.raises(ValueError):
+        oracle_lib.attention_fwd_gqa(q, k, k, False, 1.0)

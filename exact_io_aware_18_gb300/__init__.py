@@ -17,14 +17,14 @@ import torch
 
 from ._lib import (FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT, FA_ERR_INVALID_ARG, FA_ERR_MISALIGNED,
                    FA_ERR_NO_MEMORY, FA_ERR_UNSUPPORTED, FA_OK, FaError, error_string, fa_bwd,
-                   fa_bwd_dkdv, fa_bwd_dq, fa_bwd_f32, fa_bwd_noalloc, fa_bwd_preprocess,
-                   fa_bwd_workspace_bytes,
-                   fa_device_status, fa_fwd, fa_fwd_f32, fa_selftest_wait_timeout,
+                   fa_bwd_dkdv, fa_bwd_dq, fa_bwd_f32, fa_bwd_gqa, fa_bwd_noalloc,
+                   fa_bwd_preprocess, fa_bwd_workspace_bytes, fa_device_status, fa_fwd,
+                   fa_fwd_f32, fa_fwd_gqa, fa_selftest_wait_timeout,
                    fa_set_wait_timeout_ns, lib_path, load)
 
 __all__ = [
     "attention_fwd", "attention_bwd", "fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv",
-    "fa_bwd_dq", "fa_bwd_noalloc",
+    "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa",
     "fa_bwd_workspace_bytes", "fa_fwd_f32", "fa_bwd_f32", "fa_device_status",
     "fa_set_wait_timeout_ns", "fa_selftest_wait_timeout", "FaError", "error_string", "load",
     "lib_path", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
@@ -38,13 +38,19 @@ def default_scale(d: int) -> float:
 
 
 def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
-    """Allocates O and LSE and runs fa_fwd (bf16) or fa_fwd_f32 (fp32)."""
+    """Allocates O and LSE and runs fa_fwd (bf16) or fa_fwd_f32 (fp32).
+
+    With fewer K/V heads than query heads (bf16 only), grouped-query
+    attention: fa_fwd_gqa.
+    """
     B, H, N, d = q.shape
     scale = default_scale(d) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if q.dtype == torch.float32:
         fa_fwd_f32(q, k, v, o, lse, causal, scale, stream)
+    elif k.shape[1] != H:
+        fa_fwd_gqa(q, k, v, o, lse, causal, scale, stream)
     else:
         fa_fwd(q, k, v, o, lse, causal, scale, stream)
     return o, lse
@@ -52,14 +58,20 @@ def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None, str
 
 def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
                   workspace=None, stream=None):
-    """Allocates FP32 dQ, dK, dV and runs fa_bwd (bf16) or fa_bwd_f32 (fp32)."""
+    """Allocates FP32 dQ, dK, dV and runs fa_bwd (bf16) or fa_bwd_f32 (fp32).
+
+    With fewer K/V heads than query heads (bf16 only): fa_bwd_gqa, and dK, dV
+    have the K/V heads' shape.
+    """
     d = q.shape[-1]
     scale = default_scale(d) if scale is None else scale
     dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
-    dk = torch.empty_like(dq)
-    dv = torch.empty_like(dq)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty_like(dk)
     if q.dtype == torch.float32:
         fa_bwd_f32(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream)
+    elif k.shape[1] != q.shape[1]:
+        fa_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream)
     else:
         fa_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream)
     return dq, dk, dv

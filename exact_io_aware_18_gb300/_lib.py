@@ -45,6 +45,8 @@ _SIGNATURES = {
     "fa_set_wait_timeout_ns": ([ctypes.c_ulonglong], None),
     "fa_selftest_wait_timeout": ([ctypes.c_ulonglong, _vp], _i),
     "fa_bwd_noalloc": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_fwd_gqa": ([_vp] * 5 + [_i] * 6 + [_f, _vp], _i),
+    "fa_bwd_gqa": ([_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp], _i),
 }
 
 NOALLOC_SCRATCH_BYTES = 8 << 20  # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
@@ -129,6 +131,39 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
     _expect(lse, "lse", torch.float32, (B, H, N))
     _check(load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
                          int(bool(causal)), float(scale), _stream(stream)), "fa_fwd")
+
+
+def _gqa_heads(q, k):
+    B, Hq, N, d = _bhnd(q)
+    if k.dim() != 4:
+        raise ValueError("k must be [B, Hkv, N, d]")
+    return B, Hq, int(k.shape[1]), N, d
+
+
+def fa_fwd_gqa(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """Grouped-query attention forward: q, o [B,Hq,N,d]; k, v [B,Hkv,N,d]; Hkv divides Hq."""
+    B, Hq, Hkv, N, d = _gqa_heads(q, k)
+    for name, t, h in (("q", q, Hq), ("k", k, Hkv), ("v", v, Hkv), ("o", o, Hq)):
+        _expect(t, name, torch.bfloat16, (B, h, N, d))
+    _expect(lse, "lse", torch.float32, (B, Hq, N))
+    _check(load().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
+                             int(bool(causal)), float(scale), _stream(stream)), "fa_fwd_gqa")
+
+
+def fa_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, workspace=None,
+               stream=None) -> None:
+    """Grouped-query attention backward: dq [B,Hq,N,d], dk and dv [B,Hkv,N,d] (fp32)."""
+    B, Hq, Hkv, N, d = _gqa_heads(q, k)
+    for name, t, h in (("q", q, Hq), ("k", k, Hkv), ("v", v, Hkv), ("o", o, Hq), ("do", do, Hq)):
+        _expect(t, name, torch.bfloat16, (B, h, N, d))
+    _expect(lse, "lse", torch.float32, (B, Hq, N))
+    for name, t, h in (("dq", dq, Hq), ("dk", dk, Hkv), ("dv", dv, Hkv)):
+        _expect(t, name, torch.float32, (B, h, N, d))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                             _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(bool(causal)),
+                             float(scale), _ptr(workspace), ws_bytes, _stream(stream)),
+           "fa_bwd_gqa")
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

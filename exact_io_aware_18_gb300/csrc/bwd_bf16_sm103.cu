@@ -103,9 +103,9 @@ __global__ void __launch_bounds__(352, 1)
                          const __grid_constant__ CUtensorMap tm_dk,
                          const __grid_constant__ CUtensorMap tm_dv,
                          const float* __restrict__ delta, const float* __restrict__ lse2,
-                         int N, int n_pad,
-                         int BH, int n_tiles, int group, float scale, float scale_log2,
-                         unsigned int* status, unsigned long long timeout_ns) {
+                         int N, int n_pad, int BHkv, int Hkv, int n_rep, int n_tiles,
+                         int group, float scale, float scale_log2, unsigned int* status,
+                         unsigned long long timeout_ns) {
     using C = BwdCfg<D>;
     using Bar = BwdBars<C::NSQ>;
     extern __shared__ uint8_t smem_raw[];
@@ -133,11 +133,16 @@ __global__ void __launch_bounds__(352, 1)
     const long long lin = blockIdx.x + static_cast<long long>(gridDim.x) *
                                            (blockIdx.y + static_cast<long long>(gridDim.y) *
                                                              blockIdx.z);
-    const TileHead th = grouped_order(lin, BH, n_tiles, group, false);
+    const TileHead th = grouped_order(lin, BHkv, n_tiles, group, false);
     const int kt = th.tile;
-    const int bh = th.head;
+    const int bkv = th.head;  // K/V head (b * Hkv + j)
     const int i0 = CAUSAL ? kt : 0;
     const int n_q = n_tiles - i0;
+    // Step t covers query head r = t / n_q of this K/V head's group (the
+    // n_rep query heads b * Hq + j * n_rep + r, Hq = n_rep * Hkv) and its Q
+    // tile i = i0 + t % n_q; with n_rep = 1 this is plain multi-head attention.
+    const int n_steps = n_rep * n_q;
+    const int bhq0 = (bkv / Hkv) * (Hkv * n_rep) + (bkv % Hkv) * n_rep;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -176,7 +181,8 @@ __global__ void __launch_bounds__(352, 1)
         if (lane == 0) {
             auto load_tile = [&](int t) {
                 const int st = t % C::NSQ;
-                const int i = i0 + t;
+                const int i = i0 + t % n_q;
+                const int bh = bhq0 + t / n_q;  // query head
                 const uint32_t fb = bar(Bar::Q_FULL + st);
                 mbar_arrive_expect_tx(fb, C::STAGE_BYTES + 1024);
                 for (int kb = 0; kb < C::KB; ++kb) {
@@ -191,12 +197,12 @@ __global__ void __launch_bounds__(352, 1)
             mbar_arrive_expect_tx(bar(Bar::KV_FULL), 2 * C::TILE_BYTES);
             for (int kb = 0; kb < C::KB; ++kb) {
                 tma_load_3d(s_k + kb * C::BOX_BYTES, &tm_k, bar(Bar::KV_FULL), kb * 64,
-                            kt * C::BN, bh);
+                            kt * C::BN, bkv);
                 tma_load_3d(s_v + kb * C::BOX_BYTES, &tm_v, bar(Bar::KV_FULL), kb * 64,
-                            kt * C::BN, bh);
+                            kt * C::BN, bkv);
             }
             int issued = 0;
-            for (; issued < n_q; ++issued) {
+            for (; issued < n_steps; ++issued) {
                 const int use = issued / C::NSQ;
                 if (use > 0 &&
                     !mbar_wait(bar(Bar::Q_EMPTY + issued % C::NSQ), (use - 1) & 1, wc))
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(352, 1)
                 return true;
             };
             bool ok = mbar_wait(bar(Bar::KV_FULL), 0, wc) && issue_first(0);
-            for (int t = 0; t < n_q && ok; ++t) {
+            for (int t = 0; t < n_steps && ok; ++t) {
                 const int st = t % C::NSQ;
                 ok = mbar_wait(bar(ready_bar), t & 1, wc);
                 if (!ok) break;
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(352, 1)
                            id_kv, (t > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar(Bar::Q_EMPTY + st));  // this issuer no longer reads stage t
-                if (t + 1 < n_q) ok = issue_first(t + 1);
+                if (t + 1 < n_steps) ok = issue_first(t + 1);
             }
             if (ok) tc_commit(bar(Bar::ACC_FULL));
         }
@@ -272,9 +278,9 @@ __global__ void __launch_bounds__(352, 1)
         const float* vec_base = reinterpret_cast<const float*>(smem + C::OFF_VEC);
         const bool key_pad = kglob >= N;
         bool ok = true;
-        for (int t = 0; t < n_q; ++t) {
+        for (int t = 0; t < n_steps; ++t) {
             const int st = t % C::NSQ;
-            const int i = i0 + t;
+            const int i = i0 + t % n_q;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_FULL), t & 1, wc) &&
                                              mbar_wait(bar(Bar::Q_FULL + st),
                                                        (t / C::NSQ) & 1, wc));
@@ -356,9 +362,9 @@ __global__ void __launch_bounds__(352, 1)
             if (lane == 0 && row0 < N) {
 #pragma unroll
                 for (int ch = 0; ch < D / 64; ++ch) {
-                    tma_store_3d(&tm_dv, stg + ch * 4096, (D / 2) * h + ch * 32, row0, bh);
+                    tma_store_3d(&tm_dv, stg + ch * 4096, (D / 2) * h + ch * 32, row0, bkv);
                     tma_store_3d(&tm_dk, stg + kHalfBytes + ch * 4096, (D / 2) * h + ch * 32,
-                                 row0, bh);
+                                 row0, bkv);
                 }
                 bulk_commit();
                 bulk_wait_read_all();  // the boxes stay in place until read
@@ -392,10 +398,11 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     // Enough heads per group that a group fills about one wave of CTAs.
     int group = 128 / n_tiles;
     if (group < 1) group = 1;
-    dim3 grid(n_tiles, a.H, a.B);
+    dim3 grid(n_tiles, a.Hkv, a.B);  // one CTA per key tile of each K/V head
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
         *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dk, *a.tm_dv, a.delta, a.lse2, a.N, a.n_pad,
-        a.B * a.H, n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
+        a.B * a.Hkv, a.Hkv, a.H / a.Hkv, n_tiles, group, a.scale, a.scale_log2, a.status,
+        a.timeout_ns);
     return cudaGetLastError();
 }
 

@@ -94,7 +94,8 @@ __global__ void __launch_bounds__(384, 1)
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dq,
-                       const float* __restrict__ delta, const float* __restrict__ lse2, int N, int n_pad, int BH, int n_tiles, int group,
+                       const float* __restrict__ delta, const float* __restrict__ lse2, int N, int n_pad, int BH,
+                       int Hq, int n_rep, int n_tiles, int group,
                        float scale, float scale_log2, unsigned int* status,
                        unsigned long long timeout_ns) {
     using C = DqCfg<D>;
@@ -123,6 +124,8 @@ __global__ void __launch_bounds__(384, 1)
     const TileHead th = grouped_order(lin, BH, n_tiles, group, true);
     const int qt = th.tile;
     const int bh = th.head;
+    // K/V head of query head bh: its group's head (b * Hkv + h / n_rep).
+    const int bkv = (bh / Hq) * (Hq / n_rep) + (bh % Hq) / n_rep;
     const int n_kv = CAUSAL ? qt + 1 : n_tiles;
 
     const int warp = threadIdx.x >> 5;
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(384, 1)
                 mbar_arrive_expect_tx(bar(Bar::K_FULL + st), C::TILE_BYTES);
                 for (int kb = 0; kb < C::KB; ++kb)
                     tma_load_3d(s_k + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_k,
-                                bar(Bar::K_FULL + st), kb * 64, issued * C::BN, bh);
+                                bar(Bar::K_FULL + st), kb * 64, issued * C::BN, bkv);
             }
             mbar_wait_drain(bar(Bar::QD_FULL), 0, timeout_ns);
             for (int j = (issued > C::NSK ? issued - C::NSK : 0); j < issued; ++j)
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(384, 1)
                 mbar_arrive_expect_tx(bar(Bar::V_FULL + st), C::TILE_BYTES);
                 for (int kb = 0; kb < C::KB; ++kb)
                     tma_load_3d(s_v + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_v,
-                                bar(Bar::V_FULL + st), kb * 64, issued * C::BN, bh);
+                                bar(Bar::V_FULL + st), kb * 64, issued * C::BN, bkv);
             }
             for (int j = (issued > C::NSV ? issued - C::NSV : 0); j < issued; ++j)
                 mbar_wait_drain(bar(Bar::V_FULL + j % C::NSV), (j / C::NSV) & 1, timeout_ns);
@@ -379,7 +382,7 @@ cudaError_t launch_t(const DqArgs& a, cudaStream_t stream) {
     dim3 grid(n_tiles, a.H, a.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
         *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, a.delta, a.lse2, a.N, a.n_pad, a.B * a.H,
-        n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
+        a.H, a.H / a.Hkv, n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
     return cudaGetLastError();
 }
 

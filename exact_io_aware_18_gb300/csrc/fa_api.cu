@@ -152,6 +152,86 @@ long long n_pad_of(int N) { return (static_cast<long long>(N) + 127) / 128 * 128
 
 int launch_rc(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+
+// Query heads Hq share Hkv K/V heads (grouped-query attention); Hq = Hkv is
+// multi-head attention.
+int check_heads(int Hq, int Hkv) {
+    if (Hkv < 1 || Hkv > Hq || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int N, int d, int causal, float scale, void* stream) {
+    if (int rc = check_ptrs({q, k, v, o, lse})) return rc;
+    if (int rc = check_shape(B, Hq, N, d, scale)) return rc;
+    if (int rc = check_heads(Hq, Hkv)) return rc;
+    unsigned int* status;
+    if (int rc = status_ptr(&status)) return rc;
+    const long long BH = static_cast<long long>(B) * Hq;
+    const long long BHkv = static_cast<long long>(B) * Hkv;
+    CUtensorMap tq, tk, tv, to;
+    if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tk, k, d, N, BHkv)) return rc;
+    if (int rc = make_map_bf16(&tv, v, d, N, BHkv)) return rc;
+    if (int rc = make_map_bf16(&to, o, d, N, BH)) return rc;
+    unsigned int* work;
+    int sms;
+    if (int rc = work_slot(&work, &sms)) return rc;
+    fa::FwdArgs a{&tq, &tk, &tv, &to, lse, B, Hq, N, d, Hkv, causal ? 1 : 0,
+                  scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms};
+    return launch_rc(fa::launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)));
+}
+
+int dkdv_impl(const void* q, const void* k, const void* v, const void* do_,
+              const float* delta_ws, const float* lse2_ws, float* dk, float* dv, int B, int Hq,
+              int Hkv, int N, int d, int causal, float scale, void* stream) {
+    if (int rc = check_ptrs({q, k, v, do_, delta_ws, lse2_ws, dk, dv})) return rc;
+    if (int rc = check_shape(B, Hq, N, d, scale)) return rc;
+    if (int rc = check_heads(Hq, Hkv)) return rc;
+    unsigned int* status;
+    if (int rc = status_ptr(&status)) return rc;
+    const long long BH = static_cast<long long>(B) * Hq;
+    const long long BHkv = static_cast<long long>(B) * Hkv;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tk, k, d, N, BHkv)) return rc;
+    if (int rc = make_map_bf16(&tv, v, d, N, BHkv)) return rc;
+    if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
+    if (int rc = make_map_f32_out(&tdk, dk, d, N, BHkv)) return rc;
+    if (int rc = make_map_f32_out(&tdv, dv, d, N, BHkv)) return rc;
+    fa::BwdArgs a{&tq, &tk, &tv, &tdo, &tdk, &tdv, delta_ws, lse2_ws, B, Hq, N, d,
+                  static_cast<int>(n_pad_of(N)), Hkv, causal ? 1 : 0, scale,
+                  scale * 1.4426950408889634f, status, g_timeout_ns.load()};
+    return launch_rc(fa::launch_bwd_dkdv_bf16(a, static_cast<cudaStream_t>(stream)));
+}
+
+int dq_impl(const void* q, const void* k, const void* v, const void* do_, const float* delta_ws,
+            const float* lse2_ws, float* dq, int B, int Hq, int Hkv, int N, int d, int causal,
+            float scale, void* stream) {
+    if (int rc = check_ptrs({q, k, v, do_, delta_ws, lse2_ws, dq})) return rc;
+    if (int rc = check_shape(B, Hq, N, d, scale)) return rc;
+    if (int rc = check_heads(Hq, Hkv)) return rc;
+    unsigned int* status;
+    if (int rc = status_ptr(&status)) return rc;
+    const long long BH = static_cast<long long>(B) * Hq;
+    const long long BHkv = static_cast<long long>(B) * Hkv;
+    CUtensorMap tq, tk, tv, tdo, tdq;
+    if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
+    if (int rc = make_map_bf16(&tk, k, d, N, BHkv)) return rc;
+    if (int rc = make_map_bf16(&tv, v, d, N, BHkv)) return rc;
+    if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
+    if (int rc = make_map_f32_out(&tdq, dq, d, N, BH)) return rc;
+    fa::DqArgs a{&tq, &tk, &tv, &tdo, &tdq, delta_ws, lse2_ws, B, Hq, N, d,
+                 static_cast<int>(n_pad_of(N)), Hkv, causal ? 1 : 0, scale,
+                 scale * 1.4426950408889634f, status, g_timeout_ns.load()};
+    return launch_rc(fa::launch_bwd_dq_bf16(a, static_cast<cudaStream_t>(stream)));
+}
+
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* do_,
+             const float* lse, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int N,
+             int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+             void* stream);
+
 }  // namespace
 
 extern "C" {
@@ -188,22 +268,12 @@ int fa_device_status(int clear) {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, int causal, float scale, void* stream) {
-    if (int rc = check_ptrs({q, k, v, o, lse})) return rc;
-    if (int rc = check_shape(B, H, N, d, scale)) return rc;
-    unsigned int* status;
-    if (int rc = status_ptr(&status)) return rc;
-    const long long BH = static_cast<long long>(B) * H;
-    CUtensorMap tq, tk, tv, to;
-    if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
-    if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
-    if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
-    if (int rc = make_map_bf16(&to, o, d, N, BH)) return rc;
-    unsigned int* work;
-    int sms;
-    if (int rc = work_slot(&work, &sms)) return rc;
-    fa::FwdArgs a{&tq, &tk, &tv, &to, lse, B, H, N, d, causal ? 1 : 0,
-                  scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms};
-    return launch_rc(fa::launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)));
+    return fwd_impl(q, k, v, o, lse, B, H, H, N, d, causal, scale, stream);
+}
+
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+               int Hkv, int N, int d, int causal, float scale, void* stream) {
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -225,67 +295,29 @@ int fa_bwd_preprocess(const void* o, const void* do_, const float* lse, float* d
 int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
                 const float* delta_ws, const float* lse2_ws, float* dk, float* dv, int B, int H,
                 int N, int d, int causal, float scale, void* stream) {
-    if (int rc = check_ptrs({q, k, v, do_, delta_ws, lse2_ws, dk, dv})) return rc;
-    if (int rc = check_shape(B, H, N, d, scale)) return rc;
-    unsigned int* status;
-    if (int rc = status_ptr(&status)) return rc;
-    const long long BH = static_cast<long long>(B) * H;
-    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-    if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
-    if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
-    if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
-    if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
-    if (int rc = make_map_f32_out(&tdk, dk, d, N, BH)) return rc;
-    if (int rc = make_map_f32_out(&tdv, dv, d, N, BH)) return rc;
-    fa::BwdArgs a{&tq, &tk, &tv, &tdo, &tdk, &tdv, delta_ws, lse2_ws, B, H, N, d,
-                  static_cast<int>(n_pad_of(N)), causal ? 1 : 0, scale,
-                  scale * 1.4426950408889634f, status, g_timeout_ns.load()};
-    return launch_rc(fa::launch_bwd_dkdv_bf16(a, static_cast<cudaStream_t>(stream)));
+    return dkdv_impl(q, k, v, do_, delta_ws, lse2_ws, dk, dv, B, H, H, N, d, causal, scale,
+                     stream);
 }
 
 int fa_bwd_dq(const void* q, const void* k, const void* v, const void* do_,
               const float* delta_ws, const float* lse2_ws, float* dq, int B, int H, int N, int d,
               int causal, float scale, void* stream) {
-    if (int rc = check_ptrs({q, k, v, do_, delta_ws, lse2_ws, dq})) return rc;
-    if (int rc = check_shape(B, H, N, d, scale)) return rc;
-    unsigned int* status;
-    if (int rc = status_ptr(&status)) return rc;
-    const long long BH = static_cast<long long>(B) * H;
-    CUtensorMap tq, tk, tv, tdo, tdq;
-    if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
-    if (int rc = make_map_bf16(&tk, k, d, N, BH)) return rc;
-    if (int rc = make_map_bf16(&tv, v, d, N, BH)) return rc;
-    if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
-    if (int rc = make_map_f32_out(&tdq, dq, d, N, BH)) return rc;
-    fa::DqArgs a{&tq, &tk, &tv, &tdo, &tdq, delta_ws, lse2_ws, B, H, N, d,
-                 static_cast<int>(n_pad_of(N)), causal ? 1 : 0, scale,
-                 scale * 1.4426950408889634f, status, g_timeout_ns.load()};
-    return launch_rc(fa::launch_bwd_dq_bf16(a, static_cast<cudaStream_t>(stream)));
+    return dq_impl(q, k, v, do_, delta_ws, lse2_ws, dq, B, H, H, N, d, causal, scale, stream);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_,
            const float* lse, float* dq, float* dk, float* dv, int B, int H, int N, int d,
            int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
-    if (int rc = check_ptrs({q, k, v, o, do_, lse, dq, dk, dv})) return rc;
-    if (int rc = check_shape(B, H, N, d, scale)) return rc;
-    const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    void* ws = workspace;
-    if (ws) {
-        if (!aligned16(ws)) return FA_ERR_MISALIGNED;
-        if (workspace_bytes < need) return FA_ERR_NO_MEMORY;
-    } else if (cudaMallocAsync(&ws, need, s) != cudaSuccess) {
-        return FA_ERR_NO_MEMORY;
-    }
-    float* delta = static_cast<float*>(ws);
-    float* lse2 = delta + static_cast<size_t>(B) * H * n_pad_of(N);
-    int rc = fa_bwd_preprocess(o, do_, lse, delta, lse2, B, H, N, d, stream);
-    if (rc == FA_OK)
-        rc = fa_bwd_dkdv(q, k, v, do_, delta, lse2, dk, dv, B, H, N, d, causal, scale, stream);
-    if (rc == FA_OK)
-        rc = fa_bwd_dq(q, k, v, do_, delta, lse2, dq, B, H, N, d, causal, scale, stream);
-    if (!workspace && cudaFreeAsync(ws, s) != cudaSuccess && rc == FA_OK) rc = FA_ERR_CUDA;
-    return rc;
+    return bwd_impl(q, k, v, o, do_, lse, dq, dk, dv, B, H, H, N, d, causal, scale, workspace,
+                    workspace_bytes, stream);
+}
+
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* do_,
+               const float* lse, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int N,
+               int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+               void* stream) {
+    return bwd_impl(q, k, v, o, do_, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale,
+                    workspace, workspace_bytes, stream);
 }
 
 int fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
@@ -343,3 +375,34 @@ int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
 }
 
 }  // extern "C"
+
+namespace {
+
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* do_,
+             const float* lse, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int N,
+             int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+             void* stream) {
+    if (int rc = check_ptrs({q, k, v, o, do_, lse, dq, dk, dv})) return rc;
+    if (int rc = check_shape(B, Hq, N, d, scale)) return rc;
+    if (int rc = check_heads(Hq, Hkv)) return rc;
+    const size_t need = fa_bwd_workspace_bytes(B, Hq, N, d);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* ws = workspace;
+    if (ws) {
+        if (!aligned16(ws)) return FA_ERR_MISALIGNED;
+        if (workspace_bytes < need) return FA_ERR_NO_MEMORY;
+    } else if (cudaMallocAsync(&ws, need, s) != cudaSuccess) {
+        return FA_ERR_NO_MEMORY;
+    }
+    float* delta = static_cast<float*>(ws);
+    float* lse2 = delta + static_cast<size_t>(B) * Hq * n_pad_of(N);
+    int rc = fa_bwd_preprocess(o, do_, lse, delta, lse2, B, Hq, N, d, stream);
+    if (rc == FA_OK)
+        rc = dkdv_impl(q, k, v, do_, delta, lse2, dk, dv, B, Hq, Hkv, N, d, causal, scale, stream);
+    if (rc == FA_OK)
+        rc = dq_impl(q, k, v, do_, delta, lse2, dq, B, Hq, Hkv, N, d, causal, scale, stream);
+    if (!workspace && cudaFreeAsync(ws, s) != cudaSuccess && rc == FA_OK) rc = FA_ERR_CUDA;
+    return rc;
+}
+
+}  // namespace

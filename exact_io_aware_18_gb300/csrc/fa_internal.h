@@ -17,7 +17,8 @@ struct FwdArgs {
     const CUtensorMap* tm_v;
     const CUtensorMap* tm_o;
     float* lse;
-    int B, H, N, d;
+    int B, H, N, d;    // H query heads
+    int Hkv;           // K/V heads, H = n_rep * Hkv (grouped-query attention)
     int causal;
     float scale_log2;  // scale * log2(e)
     unsigned int* status;
@@ -52,7 +53,8 @@ struct BwdArgs {
     const CUtensorMap* tm_dv;
     const float* delta;
     const float* lse2;
-    int B, H, N, d, n_pad;
+    int B, H, N, d, n_pad;  // H query heads
+    int Hkv;                // K/V heads, H = n_rep * Hkv
     int causal;
     float scale;       // multiplies dS (dQ = dS K, dK = dS^T Q with dS scaled)
     float scale_log2;  // scale * log2(e), for recomputing P
@@ -72,7 +74,8 @@ struct DqArgs {
     const CUtensorMap* tm_dq;
     const float* delta;
     const float* lse2;
-    int B, H, N, d, n_pad;
+    int B, H, N, d, n_pad;  // H query heads
+    int Hkv;                // K/V heads, H = n_rep * Hkv
     int causal;
     float scale;
     float scale_log2;

@@ -121,8 +121,8 @@ __global__ void __launch_bounds__(384, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, float* __restrict__ lse, int N,
-                    int BH, int n_tiles, int group, float scale_log2, unsigned int* status,
-                    unsigned long long timeout_ns, unsigned int* work) {
+                    int BH, int Hq, int n_rep, int n_tiles, int group, float scale_log2,
+                    unsigned int* status, unsigned long long timeout_ns, unsigned int* work) {
     using C = FwdCfg<D>;
     using Bar = FwdBars<C::NS, C::QUEUE>;
     static_assert(8 * Bar::COUNT + 8 <= C::BAR_BYTES, "barrier area");
@@ -269,6 +269,8 @@ __global__ void __launch_bounds__(384, 1)
                     if (item < 0) break;
                     const TileHead th = tile_of(item);
                     const int n_kv = CAUSAL ? th.tile + 1 : n_tiles;
+                    // K/V head of query head th.head: its group's head.
+                    const int bkv = (th.head / Hq) * (Hq / n_rep) + (th.head % Hq) / n_rep;
                     for (int j = 0; j < n_kv && ok; ++j, ++g) {
                         const int st = g % C::NS;
                         const int use = g / C::NS;
@@ -277,14 +279,14 @@ __global__ void __launch_bounds__(384, 1)
                         mbar_arrive_expect_tx(bar(Bar::K_FULL + st), C::TILE_BYTES);
                         for (int kb = 0; kb < C::KB; ++kb)
                             tma_load_3d(s_k + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_k,
-                                        bar(Bar::K_FULL + st), kb * 64, j * C::BN, th.head);
+                                        bar(Bar::K_FULL + st), kb * 64, j * C::BN, bkv);
                         k_issued = g + 1;
                         if (use > 0) ok = mbar_wait(bar(Bar::V_EMPTY + st), (use - 1) & 1, wc);
                         if (!ok) break;
                         mbar_arrive_expect_tx(bar(Bar::V_FULL + st), C::TILE_BYTES);
                         for (int kb = 0; kb < C::KB; ++kb)
                             tma_load_3d(s_v + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_v,
-                                        bar(Bar::V_FULL + st), kb * 64, j * C::BN, th.head);
+                                        bar(Bar::V_FULL + st), kb * 64, j * C::BN, bkv);
                         v_issued = g + 1;
                     }
                     if (ok) mbar_arrive(bar(Bar::CLAIM_OK));  // the next tile may be claimed
@@ -588,8 +590,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     const long long n_items = static_cast<long long>(a.B) * a.H * n_tiles;
     const int grid = static_cast<int>(n_items < a.num_sms ? n_items : a.num_sms);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse, a.N, a.B * a.H, n_tiles, group, a.scale_log2,
-        a.status, a.timeout_ns, a.work);
+        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse, a.N, a.B * a.H, a.H, a.H / a.Hkv, n_tiles,
+        group, a.scale_log2, a.status, a.timeout_ns, a.work);
     return cudaGetLastError();
 }
 

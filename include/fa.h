@@ -62,12 +62,12 @@ typedef enum {
  * d must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).  N may be any value
  * >= 1: the ragged last tile is masked.  B, H <= 65535.
  *
- * Each CTA owns one 128-row Q tile of one (b, h) and streams the 128-key
- * K/V tiles through a shared-memory ring ("FlashAttention scaling, multi-GPU
- * training and weight quantization", section 1: loop order with Q outside,
- * parallelism over the sequence, asynchronous TMA copies); the 1/l
- * normalisation is applied once at the end ("FlashAttention-2", technical
- * architecture, improvement 1). */
+ * One persistent CTA per SM takes 128-row Q tiles of (b, h) in turn and
+ * streams the 128-key K/V tiles through a shared-memory ring ("FlashAttention
+ * scaling, multi-GPU training and weight quantization", section 1: loop order
+ * with Q outside, parallelism over the sequence, asynchronous TMA copies);
+ * the 1/l normalisation is applied once at the end ("FlashAttention-2",
+ * technical architecture, improvement 1). */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, int causal, float scale, void* stream);
 
@@ -79,7 +79,7 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *
  * q, k, v, o, do_ : const bf16 [B,H,N,d]  (o and lse as written by fa_fwd);
  * lse             : const float [B,H,N];
- * dq, dk, dv      : float [B,H,N,d] (written; dq is zeroed then accumulated).
+ * dq, dk, dv      : float [B,H,N,d] (written).
  * workspace       : device buffer of at least fa_bwd_workspace_bytes() bytes,
  *                   16-byte aligned, or NULL: the library then allocates and
  *                   frees it on the stream (cudaMallocAsync / cudaFreeAsync).
@@ -116,6 +116,25 @@ int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
 int fa_bwd_dq(const void* q, const void* k, const void* v, const void* do_,
               const float* delta_ws, const float* lse2_ws, float* dq,
               int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/* Grouped-query attention ("FlashAttention-2", variants: multi-query and
+ * grouped-query attention): Hq query heads share Hkv K/V heads, Hq = g * Hkv,
+ * and query head h attends with K/V head h / g (Hkv = 1 is multi-query
+ * attention; Hkv = Hq is fa_fwd / fa_bwd).  Hkv must divide Hq, else
+ * FA_ERR_INVALID_ARG.
+ *
+ * q, o, do_, dq : [B,Hq,N,d];  k, v, dk, dv : [B,Hkv,N,d];  lse : [B,Hq,N].
+ * Types, workspace (fa_bwd_workspace_bytes(B, Hq, N, d)), errors and
+ * determinism as for fa_fwd / fa_bwd.  The K/V tile loads of the forward
+ * and the dQ step read the group's head; the dK/dV step runs one CTA per key
+ * tile of each K/V head and sums over the Q tiles of all g query heads, so
+ * dk and dv are still written once. */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* do_,
+               const float* lse, float* dq, float* dk, float* dv,
+               int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Size of the scratch array built into the library for fa_bwd_noalloc:
  * 8 MiB, i.e. B * H * roundup(N, 128) <= 1048576. */

@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("fa_fwd", "fa_bwd", "fa_fwd_f32", "fa_bwd_f32", "fa_bwd_workspace_bytes",
                  "fa_error_string", "fa_device_status", "fa_bwd_preprocess", "fa_bwd_dkdv",
-                 "fa_bwd_dq"):
+                 "fa_bwd_dq", "fa_fwd_gqa", "fa_bwd_gqa"):
         assert must in names
 
 
@@ -105,3 +105,17 @@ def test_binding_rejects_cpu_tensors(fa):
     lse = torch.zeros(1, 1, 8)
     with pytest.raises(ValueError):
         fa.fa_fwd(q, q, q, q, lse, False, 0.125)
+
+
+def test_gqa_head_counts_are_checked_before_launch(fa):
+    lib = fa.load()
+    p = [0x10000] * 5
+    # Hkv must divide Hq and lie in [1, Hq]
+    for hq, hkv in ((4, 3), (2, 4), (4, 0), (4, -1)):
+        assert lib.fa_fwd_gqa(*p, 1, hq, hkv, 16, 64, 1, 0.125, None) == fa.FA_ERR_INVALID_ARG
+        assert lib.fa_bwd_gqa(*([0x10000] * 9), 1, hq, hkv, 16, 64, 1, 0.125, None, 0,
+                              None) == fa.FA_ERR_INVALID_ARG
+    # the other checks still come first: misaligned pointer, bad head dimension
+    assert lib.fa_fwd_gqa(*p[:4], 0x10004, 1, 4, 2, 16, 64, 1, 0.125,
+                          None) == fa.FA_ERR_MISALIGNED
+    assert lib.fa_fwd_gqa(*p, 1, 4, 2, 16, 96, 1, 0.125, None) == fa.FA_ERR_UNSUPPORTED

@@ -1,0 +1,116 @@
+"""GPU parity for grouped-query attention (GQA, and MQA with one K/V head)
+against the FP64 oracle's definition: query head h attends with K/V head
+h // (Hq / Hkv), and dK, dV of a K/V head sum over its group of query heads.
+
+Every output is compared element by element, at shapes that span several
+tiles, a ragged last tile and, in the dK/dV step, loops that cross from one
+query head of a group to the next.  Calls go through the C ABI
+(fa_fwd_gqa / fa_bwd_gqa).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from helpers import (BF16_GRAD_MAX_ABS, BF16_GRAD_REL_RMS, BF16_LSE_MAX_ABS, BF16_O_MAX_ABS,
+                     BF16_O_REL_RMS, inputs, max_abs, rel_rms, scale_for, to_device_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_io_aware_18_gb300 as pkg
+    pkg.fa_set_wait_timeout_ns(1_000_000_000)
+    pkg.fa_device_status(clear=True)
+    yield pkg
+    assert pkg.fa_device_status(clear=True) == pkg.FA_OK
+
+
+def _gqa_inputs(seed, B, Hq, Hkv, N, d):
+    """Q and dO with Hq heads; K and V: the first Hkv heads of a draw of Hq."""
+    x = inputs(seed, B, Hq, N, d)
+    for n in ("k", "v"):
+        x[n] = np.ascontiguousarray(x[n][:, :Hkv])
+        x[n + "_bits"] = np.ascontiguousarray(x[n + "_bits"][:, :Hkv])
+    return x
+
+
+def _run(fa, x, causal, s):
+    import torch
+    dev = torch.device("cuda:0")
+    q, k, v, do = (to_device_bf16(x[n + "_bits"], dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, causal=causal, scale=s)
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, do, lse, causal=causal, scale=s)
+    torch.cuda.synchronize()
+    return [t.float().cpu().numpy() for t in (o, lse, dq, dk, dv)]
+
+
+CASES = [  # B, Hq, Hkv, N, d, causal
+    (2, 8, 2, 300, 128, True),
+    (1, 8, 2, 1000, 128, False),
+    (1, 4, 1, 257, 64, False),   # multi-query
+    (1, 6, 3, 129, 64, True),
+    (2, 4, 1, 640, 128, True),   # multi-query, several key tiles per head
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal", CASES)
+def test_gqa_matches_oracle(fa, B, Hq, Hkv, N, d, causal):
+    x = _gqa_inputs(500 + N + Hq, B, Hq, Hkv, N, d)
+    s = scale_for(d)
+    o, lse, dq, dk, dv = _run(fa, x, causal, s)
+    ro, rl = oracle.attention_fwd_gqa(x["q"], x["k"], x["v"], causal, s)
+    assert max_abs(o, ro) <= BF16_O_MAX_ABS
+    assert rel_rms(o, ro) <= BF16_O_REL_RMS
+    assert max_abs(lse, rl) <= BF16_LSE_MAX_ABS
+    rdq, rdk, rdv, _ = oracle.attention_bwd_gqa(x["q"], x["k"], x["v"], x["do"], causal, s,
+                                                o_storage="bf16")
+    assert dk.shape == (B, Hkv, N, d) and dv.shape == (B, Hkv, N, d)
+    # dK and dV of a K/V head sum the gradients of its g query heads, each with
+    # the rounding the per-head bound covers, so their max-abs bound is g times
+    # the per-head one; dQ (one query head) and the relative RMS keep theirs.
+    g = Hq // Hkv
+    for name, got, ref, bound in (("dq", dq, rdq, BF16_GRAD_MAX_ABS),
+                                  ("dk", dk, rdk, g * BF16_GRAD_MAX_ABS),
+                                  ("dv", dv, rdv, g * BF16_GRAD_MAX_ABS)):
+        assert max_abs(got, ref) <= bound, name
+        assert rel_rms(got, ref) <= BF16_GRAD_REL_RMS, name
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal", [(2, 8, 2, 300, 128, True), (1, 4, 1, 257, 64, False)])
+def test_gqa_equals_mha_on_repeated_kv(fa, B, Hq, Hkv, N, d, causal):
+    """The grouped path against the multi-head path on K, V repeated per query
+    head: O, LSE and dQ identical, dK and dV the group sums (up to the FP32
+    order of the sum)."""
+    import torch
+    dev = torch.device("cuda:0")
+    x = _gqa_inputs(600 + N, B, Hq, Hkv, N, d)
+    s = scale_for(d)
+    g = Hq // Hkv
+    q, k, v, do = (to_device_bf16(x[n + "_bits"], dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, causal=causal, scale=s)
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, do, lse, causal=causal, scale=s)
+    kr = k.repeat_interleave(g, dim=1).contiguous()
+    vr = v.repeat_interleave(g, dim=1).contiguous()
+    o2, lse2 = fa.attention_fwd(q, kr, vr, causal=causal, scale=s)
+    dq2, dk2, dv2 = fa.attention_bwd(q, kr, vr, o2, do, lse2, causal=causal, scale=s)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2) and torch.equal(dq, dq2)
+    for got, full in ((dk, dk2), (dv, dv2)):
+        ref = full.view(B, Hkv, g, N, d).sum(2)
+        assert (got - ref).abs().max().item() <= 1e-4 * max(1.0, ref.abs().max().item())
+
+
+def test_gqa_backward_is_deterministic(fa):
+    x = _gqa_inputs(77, 1, 8, 2, 700, 128)
+    s = scale_for(128)
+    a = _run(fa, x, True, s)
+    b = _run(fa, x, True, s)
+    for u, w in zip(a, b):
+        assert np.array_equal(u.view(np.uint32), w.view(np.uint32))

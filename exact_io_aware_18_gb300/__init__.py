@@ -19,12 +19,14 @@ from ._lib import (FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT, FA_ERR_INVALID_ARG, FA_ER
                    FA_ERR_NO_MEMORY, FA_ERR_UNSUPPORTED, FA_OK, FaError, error_string, fa_bwd,
                    fa_bwd_dkdv, fa_bwd_dq, fa_bwd_f32, fa_bwd_gqa, fa_bwd_noalloc,
                    fa_bwd_preprocess, fa_bwd_workspace_bytes, fa_device_status, fa_fwd,
-                   fa_fwd_f32, fa_fwd_gqa, fa_selftest_wait_timeout,
+                   fa_fwd_f32, fa_fwd_gqa, fa_fwd_splitkv, fa_fwd_splitkv_workspace_bytes,
+                   fa_selftest_wait_timeout,
                    fa_set_wait_timeout_ns, lib_path, load)
 
 __all__ = [
     "attention_fwd", "attention_bwd", "fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv",
-    "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa",
+    "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv",
+    "fa_fwd_splitkv_workspace_bytes", "attention_decode",
     "fa_bwd_workspace_bytes", "fa_fwd_f32", "fa_bwd_f32", "fa_device_status",
     "fa_set_wait_timeout_ns", "fa_selftest_wait_timeout", "FaError", "error_string", "load",
     "lib_path", "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
@@ -53,6 +55,18 @@ def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None, str
         fa_fwd_gqa(q, k, v, o, lse, causal, scale, stream)
     else:
         fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def attention_decode(q, k, v, scale: float | None = None, n_splits: int = 0, workspace=None,
+                     stream=None):
+    """Allocates O and LSE and runs fa_fwd_splitkv: few queries [B,Hq,Nq,d] against
+    many keys [B,Hkv,Nk,d], every query reading every key."""
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd_splitkv(q, k, v, o, lse, scale, n_splits, workspace, stream)
     return o, lse
 
 

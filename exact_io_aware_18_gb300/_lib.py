@@ -47,6 +47,8 @@ _SIGNATURES = {
     "fa_bwd_noalloc": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_fwd_gqa": ([_vp] * 5 + [_i] * 6 + [_f, _vp], _i),
     "fa_bwd_gqa": ([_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp], _i),
+    "fa_fwd_splitkv_workspace_bytes": ([_i] * 6, _sz),
+    "fa_fwd_splitkv": ([_vp] * 5 + [_i] * 6 + [_f, _i, _vp, _sz, _vp], _i),
 }
 
 NOALLOC_SCRATCH_BYTES = 8 << 20  # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
@@ -164,6 +166,30 @@ def fa_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, work
                              _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(bool(causal)),
                              float(scale), _ptr(workspace), ws_bytes, _stream(stream)),
            "fa_bwd_gqa")
+
+
+def fa_fwd_splitkv_workspace_bytes(B: int, Hq: int, Nq: int, Nk: int, d: int,
+                                   n_splits: int = 0) -> int:
+    return int(load().fa_fwd_splitkv_workspace_bytes(int(B), int(Hq), int(Nq), int(Nk), int(d),
+                                                     int(n_splits)))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, scale: float, n_splits: int = 0, workspace=None,
+                   stream=None) -> None:
+    """Decode forward: q, o [B,Hq,Nq,d]; k, v [B,Hkv,Nk,d] (bf16); no mask; the keys
+    are cut into n_splits chunks (<= 0: the library's choice) merged at the end."""
+    B, Hq, Nq, d = _bhnd(q)
+    if k.dim() != 4:
+        raise ValueError("k must be [B, Hkv, Nk, d]")
+    Hkv, Nk = int(k.shape[1]), int(k.shape[2])
+    for name, t, shape in (("q", q, (B, Hq, Nq, d)), ("k", k, (B, Hkv, Nk, d)),
+                           ("v", v, (B, Hkv, Nk, d)), ("o", o, (B, Hq, Nq, d))):
+        _expect(t, name, torch.bfloat16, shape)
+    _expect(lse, "lse", torch.float32, (B, Hq, Nq))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq,
+                                 Nk, d, float(scale), int(n_splits), _ptr(workspace), ws_bytes,
+                                 _stream(stream)), "fa_fwd_splitkv")
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

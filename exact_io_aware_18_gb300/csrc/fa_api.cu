@@ -178,7 +178,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     int sms;
     if (int rc = work_slot(&work, &sms)) return rc;
     fa::FwdArgs a{&tq, &tk, &tv, &to, lse, B, Hq, N, d, Hkv, causal ? 1 : 0,
-                  scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms};
+                  scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms,
+                  /*Nk=*/N, /*n_splits=*/1, /*chunk_tiles=*/0, nullptr, nullptr};
     return launch_rc(fa::launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -232,6 +233,37 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
              int d, int causal, float scale, void* workspace, size_t workspace_bytes,
              void* stream);
 
+// Split-KV plan: the key tiles are cut into chunks of chunk_tiles; n_splits
+// chunks, none empty.  requested <= 0 asks for enough chunks that the (head,
+// Q tile, chunk) items cover every SM twice.
+struct SplitPlan {
+    int n_splits;
+    int chunk_tiles;
+};
+
+int split_plan(int B, int Hq, int Nq, int Nk, int requested, SplitPlan* out) {
+    const long long kv_tiles = (static_cast<long long>(Nk) + 127) / 128;
+    const long long q_items = static_cast<long long>(B) * Hq * ((Nq + 127) / 128);
+    long long want = requested;
+    if (want <= 0) {
+        unsigned int* unused;
+        int sms = 0;
+        if (int rc = work_slot(&unused, &sms)) return rc;
+        want = (2LL * sms + q_items - 1) / q_items;
+    }
+    if (want < 1) want = 1;
+    if (want > kv_tiles) want = kv_tiles;
+    const long long chunk = (kv_tiles + want - 1) / want;
+    out->chunk_tiles = static_cast<int>(chunk);
+    out->n_splits = static_cast<int>((kv_tiles + chunk - 1) / chunk);
+    return FA_OK;
+}
+
+size_t splitkv_bytes(int B, int Hq, int Nq, int d, int n_splits) {
+    const size_t rows = static_cast<size_t>(B) * Hq * Nq * n_splits;
+    return rows * static_cast<size_t>(d) * 4 + rows * 4;
+}
+
 }  // namespace
 
 extern "C" {
@@ -274,6 +306,59 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                int Hkv, int N, int d, int causal, float scale, void* stream) {
     return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, stream);
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Nq, int Nk, int d, int n_splits) {
+    if (B < 1 || Hq < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
+    SplitPlan plan;
+    if (split_plan(B, Hq, Nq, Nk, n_splits, &plan) != FA_OK) return 0;
+    return splitkv_bytes(B, Hq, Nq, d, plan.n_splits);
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int Hq, int Hkv, int Nq, int Nk, int d, float scale, int n_splits,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+    if (int rc = check_ptrs({q, k, v, o, lse})) return rc;
+    if (int rc = check_shape(B, Hq, Nq, d, scale)) return rc;
+    if (int rc = check_shape(B, Hkv, Nk, d, scale)) return rc;
+    if (int rc = check_heads(Hq, Hkv)) return rc;
+    SplitPlan plan;
+    if (int rc = split_plan(B, Hq, Nq, Nk, n_splits, &plan)) return rc;
+    const size_t need = splitkv_bytes(B, Hq, Nq, d, plan.n_splits);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* ws = workspace;
+    if (ws) {
+        if (!aligned16(ws)) return FA_ERR_MISALIGNED;
+        if (workspace_bytes < need) return FA_ERR_NO_MEMORY;
+    } else if (cudaMallocAsync(&ws, need, st) != cudaSuccess) {
+        return FA_ERR_NO_MEMORY;
+    }
+    float* o_part = static_cast<float*>(ws);
+    float* lse_part = o_part + static_cast<size_t>(B) * Hq * Nq * plan.n_splits * d;
+    int rc = FA_OK;
+    unsigned int* status;
+    unsigned int* work;
+    int sms;
+    CUtensorMap tq, tk, tv;
+    const long long BH = static_cast<long long>(B) * Hq;
+    const long long BHkv = static_cast<long long>(B) * Hkv;
+    if ((rc = status_ptr(&status)) == FA_OK && (rc = work_slot(&work, &sms)) == FA_OK &&
+        (rc = make_map_bf16(&tq, q, d, Nq, BH)) == FA_OK &&
+        (rc = make_map_bf16(&tk, k, d, Nk, BHkv)) == FA_OK &&
+        (rc = make_map_bf16(&tv, v, d, Nk, BHkv)) == FA_OK) {
+        // The split kernel stores no O tile: the Q map stands in for O's.
+        fa::FwdArgs a{&tq, &tk, &tv, &tq, nullptr, B, Hq, Nq, d, Hkv, 0,
+                      scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms,
+                      Nk, plan.n_splits, plan.chunk_tiles, o_part, lse_part};
+        rc = launch_rc(fa::launch_fwd_splitkv_bf16(a, st));
+        if (rc == FA_OK) {
+            fa::CombineArgs c{o_part, lse_part, o, lse, static_cast<int>(BH), Nq, d,
+                              plan.n_splits};
+            rc = launch_rc(fa::launch_splitkv_combine(c, st));
+        }
+    }
+    if (!workspace && cudaFreeAsync(ws, st) != cudaSuccess && rc == FA_OK) rc = FA_ERR_CUDA;
+    return rc;
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {

@@ -25,9 +25,33 @@ struct FwdArgs {
     unsigned long long timeout_ns;
     unsigned int* work;  // tile counter of this launch, zero between launches
     int num_sms;         // persistent grid size
+    // Split-KV (decode): N is the number of queries, Nk the number of keys;
+    // key tiles are cut into n_splits chunks of chunk_tiles, and each (head,
+    // Q tile, chunk) writes its normalised FP32 partial O and natural-log LSE
+    // to o_part [n_splits][B*H][N][d] and lse_part [n_splits][B*H][N].  The
+    // plain forward has Nk = N, n_splits = 1 and no partial buffers.
+    int Nk;
+    int n_splits;
+    int chunk_tiles;
+    float* o_part;
+    float* lse_part;
 };
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_splitkv_bf16(const FwdArgs& a, cudaStream_t stream);
+
+// Merge of the split-KV partials: per query row, O = sum_s w_s O_s / sum_s w_s
+// and LSE = m + ln sum_s w_s with w_s = exp(LSE_s - m), m = max_s LSE_s;
+// O is written as BF16 [BH][N][d], LSE as FP32 [BH][N].
+struct CombineArgs {
+    const float* o_part;
+    const float* lse_part;
+    void* o;
+    float* lse;
+    int BH, N, d, n_splits;
+};
+
+cudaError_t launch_splitkv_combine(const CombineArgs& a, cudaStream_t stream);
 
 // Backward preprocess (BF16): D and base-2 LSE into padded [B*H, n_pad]
 // vectors.

@@ -115,14 +115,16 @@ struct FwdBars {
     static constexpr int COUNT = DONE + 1;
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, float* __restrict__ lse, int N,
                     int BH, int Hq, int n_rep, int n_tiles, int group, float scale_log2,
-                    unsigned int* status, unsigned long long timeout_ns, unsigned int* work) {
+                    unsigned int* status, unsigned long long timeout_ns, unsigned int* work,
+                    int Nk, int n_splits, int chunk_tiles, float* __restrict__ o_part,
+                    float* __restrict__ lse_part) {
     using C = FwdCfg<D>;
     using Bar = FwdBars<C::NS, C::QUEUE>;
     static_assert(8 * Bar::COUNT + 8 <= C::BAR_BYTES, "barrier area");
@@ -141,9 +143,28 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * Bar::COUNT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* items = reinterpret_cast<volatile int*>(smem + C::OFF_ITEMS);
-    const int n_items = BH * n_tiles;
-    auto tile_of = [&](int item) -> TileHead {
-        return grouped_order(item, BH, n_tiles, group, true);
+    // A work item is one Q tile of one head; with SPLIT, one Q tile of one
+    // head against one chunk of key tiles (the key chunk varies fastest).
+    const int n_items = BH * n_tiles * n_splits;
+    const int n_kv_tiles = (Nk + C::BN - 1) / C::BN;
+    struct Work {
+        int qt, bh, s;  // Q tile, query head (b * Hq + h), key chunk
+        int j0, j1;     // key tiles [j0, j1)
+    };
+    auto work_of = [&](int item) -> Work {
+        Work w;
+        w.s = SPLIT ? item % n_splits : 0;
+        const TileHead th = grouped_order(SPLIT ? item / n_splits : item, BH, n_tiles, group, true);
+        w.qt = th.tile;
+        w.bh = th.head;
+        if (SPLIT) {
+            w.j0 = w.s * chunk_tiles;
+            w.j1 = min(w.j0 + chunk_tiles, n_kv_tiles);
+        } else {
+            w.j0 = 0;
+            w.j1 = CAUSAL ? th.tile + 1 : n_kv_tiles;
+        }
+        return w;
     };
 
     const int warp = threadIdx.x >> 5;
@@ -238,11 +259,11 @@ __global__ void __launch_bounds__(384, 1)
                     items[slot] = item;
                     mbar_arrive(bar(Bar::ITEM_FULL + slot));
                     if (item < 0) break;
-                    const TileHead th = tile_of(item);
+                    const Work w = work_of(item);
                     mbar_arrive_expect_tx(bar(Bar::Q_FULL + qb), C::TILE_BYTES);
                     for (int kb = 0; kb < C::KB; ++kb)
                         tma_load_3d(s_q + qb * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_q,
-                                    bar(Bar::Q_FULL + qb), kb * 64, th.tile * C::BM, th.head);
+                                    bar(Bar::Q_FULL + qb), kb * 64, w.qt * C::BM, w.bh);
                     q_issued = k + 1;
                 }
                 // After giving up, still draw numbers until one fails, so that
@@ -267,11 +288,10 @@ __global__ void __launch_bounds__(384, 1)
                 for (int k = 0; ok; ++k) {
                     const int item = take_item(k);
                     if (item < 0) break;
-                    const TileHead th = tile_of(item);
-                    const int n_kv = CAUSAL ? th.tile + 1 : n_tiles;
-                    // K/V head of query head th.head: its group's head.
-                    const int bkv = (th.head / Hq) * (Hq / n_rep) + (th.head % Hq) / n_rep;
-                    for (int j = 0; j < n_kv && ok; ++j, ++g) {
+                    const Work w = work_of(item);
+                    // K/V head of query head w.bh: its group's head.
+                    const int bkv = (w.bh / Hq) * (Hq / n_rep) + (w.bh % Hq) / n_rep;
+                    for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
                         const int st = g % C::NS;
                         const int use = g / C::NS;
                         if (use > 0) ok = mbar_wait(bar(Bar::K_EMPTY + st), (use - 1) & 1, wc);
@@ -307,11 +327,10 @@ __global__ void __launch_bounds__(384, 1)
                 for (int k = 0; ok; ++k) {
                     const int item = take_item(k);
                     if (item < 0) break;
-                    const TileHead th = tile_of(item);
-                    const int n_kv = CAUSAL ? th.tile + 1 : n_tiles;
+                    const Work w = work_of(item);
                     if (warp == 2) {
                         // Issuer B: O += P_j V_j as soon as the softmax warps release P_j.
-                        for (int j = 0; j < n_kv && ok; ++j, ++g) {
+                        for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
                             const int st = g % C::NS;
                             ok = mbar_wait(bar(Bar::P_FULL), g & 1, wc) &&
                                  mbar_wait(bar(Bar::V_FULL + st), (g / C::NS) & 1, wc);
@@ -324,7 +343,7 @@ __global__ void __launch_bounds__(384, 1)
                                 const uint64_t bd =
                                     smem_desc_sw128(v_tile + kk * 2048, C::BOX_BYTES, 1024);
                                 mma_ts(tmem + C::COL_O, tmem + C::COL_P + kk * 8, bd, id_pv,
-                                       (j > 0 || kk > 0));
+                                       (j > w.j0 || kk > 0));
                             }
                             tc_commit(bar(Bar::V_EMPTY + st));
                             tc_commit(bar(Bar::O_FULL));
@@ -334,7 +353,7 @@ __global__ void __launch_bounds__(384, 1)
                         // warps have read S_{g-2} out of it (the next phase of that
                         // S_EMPTY needs S_g itself, so the wait cannot miss it).
                         ok = mbar_wait(bar(Bar::QT_FULL), k & 1, wc);
-                        for (int j = 0; j < n_kv && ok; ++j, ++g) {
+                        for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
                             const int st = g % C::NS;
                             const int b = g & 1;
                             if (g >= 2) ok = mbar_wait(bar(Bar::S_EMPTY + b), ((g - 2) >> 1) & 1, wc);
@@ -383,10 +402,9 @@ __global__ void __launch_bounds__(384, 1)
             __syncwarp();
             if (okq && lane == 0) mbar_arrive(bar(Bar::ITEM_EMPTY + slot));
             if (!named_bar_and(5, 256, okq && item >= 0)) break;
-            const TileHead th = tile_of(item);
-            const int qt = th.tile;
-            const int bh = th.head;
-            const int n_kv = CAUSAL ? qt + 1 : n_tiles;
+            const Work w = work_of(item);
+            const int qt = w.qt;
+            const int bh = w.bh;
             const int grow = qt * C::BM + row;  // query index inside the head
             const int qb = k & 1;
             const uint32_t q_buf = C::OFF_Q + qb * C::TILE_BYTES;
@@ -399,20 +417,20 @@ __global__ void __launch_bounds__(384, 1)
                                      (k == 0 || mbar_wait(bar(Bar::QT_EMPTY), (k - 1) & 1, wc)));
             if (ok) {
                 tc_fence_after();
-                uint32_t w[D / 4];
+                uint32_t qw[D / 4];
 #pragma unroll
                 for (int c = 0; c < D / 16; ++c) {
                     const int gc = h * (D / 16) + c;  // 16-byte chunk of the row
                     const uint4 v = *reinterpret_cast<const uint4*>(
                         smem + q_buf + (gc >> 3) * C::BOX_BYTES + row * 128 +
                         (((gc & 7) ^ (row & 7)) << 4));
-                    w[4 * c] = v.x;
-                    w[4 * c + 1] = v.y;
-                    w[4 * c + 2] = v.z;
-                    w[4 * c + 3] = v.w;
+                    qw[4 * c] = v.x;
+                    qw[4 * c + 1] = v.y;
+                    qw[4 * c + 2] = v.z;
+                    qw[4 * c + 3] = v.w;
                 }
-                if constexpr (D == 128) tmem_st32(t_lane + C::COL_Q + h * (D / 4), w);
-                else tmem_st16(t_lane + C::COL_Q + h * (D / 4), w);
+                if constexpr (D == 128) tmem_st32(t_lane + C::COL_Q + h * (D / 4), qw);
+                else tmem_st16(t_lane + C::COL_Q + h * (D / 4), qw);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -421,7 +439,7 @@ __global__ void __launch_bounds__(384, 1)
 
             float m_run = -INFINITY;  // running max, base-2 units of scale * S
             float l_run = 0.f;        // this half's running sum of 2^(x - m_run)
-            for (int j = 0; j < n_kv; ++j, ++g) {
+            for (int j = w.j0; j < w.j1; ++j, ++g) {
                 const int b = g & 1;
                 const uint32_t t_s = t_lane + (b ? C::COL_S1 : C::COL_S0) + 64 * h;
                 // A failed wait is carried to the pair barrier rather than
@@ -444,11 +462,11 @@ __global__ void __launch_bounds__(384, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(Bar::S_EMPTY + b));
                     const int key0 = j * C::BN + 64 * h;  // key index of entry 0
-                    if ((CAUSAL && j == qt) || key0 + 64 > N) {
+                    if ((CAUSAL && j == qt) || key0 + 64 > Nk) {
 #pragma unroll
                         for (int c = 0; c < 64; ++c) {
                             const int key = key0 + c;
-                            if ((CAUSAL && key > grow) || key >= N) s[c] = -INFINITY;
+                            if ((CAUSAL && key > grow) || key >= Nk) s[c] = -INFINITY;
                         }
                     }
 #pragma unroll
@@ -475,7 +493,7 @@ __global__ void __launch_bounds__(384, 1)
                     pk[e] = pack_bf16x2(p0, p1);
                 }
                 l_run = l_run * alpha + sum;
-                if (j > 0) {
+                if (j > w.j0) {
                     // PV_{j-1} has finished: the P buffer is free, and O holds
                     // the sum up to PV_{j-1}, as a rescale needs.
                     ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::O_FULL), (g - 1) & 1, wc));
@@ -484,7 +502,7 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 // P (BF16): keys [64h, 64h+64) at P columns [32h, 32h+32).
                 tmem_st32(t_lane + C::COL_P + 32 * h, pk);
-                if (__any_sync(0xffffffffu, rescale) && j > 0) {
+                if (__any_sync(0xffffffffu, rescale) && j > w.j0) {
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c) {
                         uint32_t r[32];
@@ -500,7 +518,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(Bar::P_FULL));
-                if (j == 0 && threadIdx.x == kStoreThread && pending_qb >= 0) {
+                if (j == w.j0 && threadIdx.x == kStoreThread && pending_qb >= 0) {
                     // The previous tile's O store has had a whole tile of time:
                     // wait for it to finish reading its Q buffer, then free it.
                     bulk_wait_read_all();
@@ -516,33 +534,54 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) {
                 tc_fence_after();
                 const float inv_l = 1.f / l_tot;
-                if (h == 0 && grow < N)
-                    lse[static_cast<long long>(bh) * N + grow] =
-                        (m_run + lg2_approx(l_tot)) * 0.69314718055994531f;
-                // O / l -> bf16 into this tile's Q buffer (Q is in TMEM now), in
-                // the TMA box layout: this half's d/2 columns are 32-column
-                // chunks h d/64 ... .
-                uint8_t* stage = smem + q_buf;
+                const float lse_row = (m_run + lg2_approx(l_tot)) * 0.69314718055994531f;
+                if constexpr (SPLIT) {
+                    // Partial of this key chunk: O / l and LSE in FP32, merged
+                    // later.  The TMEM loads are warp-wide; only real rows store.
+                    const long long prow = (static_cast<long long>(w.s) * BH + bh) * N + grow;
+                    if (h == 0 && grow < N) lse_part[prow] = lse_row;
+                    float4* dst = reinterpret_cast<float4*>(o_part + prow * D + (D / 2) * h);
 #pragma unroll
-                for (int cc = 0; cc < D / 64; ++cc) {
-                    const int c = h * (D / 64) + cc;  // 32-column chunk of the row
-                    uint32_t r[32];
-                    tmem_ld32(t_lane + C::COL_O + c * 32, r);
-                    const int box = c >> 1;
+                    for (int cc = 0; cc < D / 64; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(t_lane + C::COL_O + (D / 2) * h + cc * 32, r);
+                        if (grow < N) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(r[8 * u + 0]) * inv_l,
-                                          __uint_as_float(r[8 * u + 1]) * inv_l);
-                        w.y = pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv_l,
-                                          __uint_as_float(r[8 * u + 3]) * inv_l);
-                        w.z = pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv_l,
-                                          __uint_as_float(r[8 * u + 5]) * inv_l);
-                        w.w = pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv_l,
-                                          __uint_as_float(r[8 * u + 7]) * inv_l);
-                        const int chunk = ((c & 1) * 4 + u) ^ (row & 7);
-                        *reinterpret_cast<uint4*>(stage + box * C::BOX_BYTES + row * 128 +
-                                                  chunk * 16) = w;
+                            for (int u = 0; u < 8; ++u)
+                                dst[cc * 8 + u] = make_float4(
+                                    __uint_as_float(r[4 * u]) * inv_l,
+                                    __uint_as_float(r[4 * u + 1]) * inv_l,
+                                    __uint_as_float(r[4 * u + 2]) * inv_l,
+                                    __uint_as_float(r[4 * u + 3]) * inv_l);
+                        }
+                    }
+                } else {
+                    if (h == 0 && grow < N) lse[static_cast<long long>(bh) * N + grow] = lse_row;
+                    // O / l -> bf16 into this tile's Q buffer (Q is in TMEM now),
+                    // in the TMA box layout: this half's d/2 columns are
+                    // 32-column chunks h d/64 ... .
+                    uint8_t* stage = smem + q_buf;
+#pragma unroll
+                    for (int cc = 0; cc < D / 64; ++cc) {
+                        const int c = h * (D / 64) + cc;  // 32-column chunk of the row
+                        uint32_t r[32];
+                        tmem_ld32(t_lane + C::COL_O + c * 32, r);
+                        const int box = c >> 1;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            uint4 pkd;
+                            pkd.x = pack_bf16x2(__uint_as_float(r[8 * u + 0]) * inv_l,
+                                                __uint_as_float(r[8 * u + 1]) * inv_l);
+                            pkd.y = pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv_l,
+                                                __uint_as_float(r[8 * u + 3]) * inv_l);
+                            pkd.z = pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv_l,
+                                                __uint_as_float(r[8 * u + 5]) * inv_l);
+                            pkd.w = pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv_l,
+                                                __uint_as_float(r[8 * u + 7]) * inv_l);
+                            const int chunk = ((c & 1) * 4 + u) ^ (row & 7);
+                            *reinterpret_cast<uint4*>(stage + box * C::BOX_BYTES + row * 128 +
+                                                      chunk * 16) = pkd;
+                        }
                     }
                 }
                 fence_async_smem();
@@ -552,7 +591,8 @@ __global__ void __launch_bounds__(384, 1)
             // whether to go on.
             if (!named_bar_and(5, 256, ok && !*abort_flag)) break;
             if (threadIdx.x == kStoreThread) {
-                for (int kb = 0; kb < C::KB; ++kb)
+                // (SPLIT: no store; the Q buffer is released all the same.)
+                for (int kb = 0; kb < C::KB && !SPLIT; ++kb)
                     tma_store_3d(&tm_o, s_q + qb * C::TILE_BYTES + kb * C::BOX_BYTES, kb * 64,
                                  qt * C::BM, bh);
                 bulk_commit();
@@ -576,10 +616,10 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     using C = FwdCfg<D>;
-    auto kern = fwd_bf16_kernel<D, CAUSAL>;
+    auto kern = fwd_bf16_kernel<D, CAUSAL, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -587,20 +627,27 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     // Enough heads per group that a group fills about one wave of tiles.
     int group = 128 / n_tiles;
     if (group < 1) group = 1;
-    const long long n_items = static_cast<long long>(a.B) * a.H * n_tiles;
+    const long long n_items = static_cast<long long>(a.B) * a.H * n_tiles * a.n_splits;
     const int grid = static_cast<int>(n_items < a.num_sms ? n_items : a.num_sms);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
         *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse, a.N, a.B * a.H, a.H, a.H / a.Hkv, n_tiles,
-        group, a.scale_log2, a.status, a.timeout_ns, a.work);
+        group, a.scale_log2, a.status, a.timeout_ns, a.work, a.Nk, a.n_splits, a.chunk_tiles,
+        a.o_part, a.lse_part);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream) {
-    if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream)
-                                   : launch_fwd_t<64, false>(a, stream);
-    return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+    if (a.d == 64) return a.causal ? launch_fwd_t<64, true, false>(a, stream)
+                                   : launch_fwd_t<64, false, false>(a, stream);
+    return a.causal ? launch_fwd_t<128, true, false>(a, stream)
+                    : launch_fwd_t<128, false, false>(a, stream);
+}
+
+cudaError_t launch_fwd_splitkv_bf16(const FwdArgs& a, cudaStream_t stream) {
+    return a.d == 64 ? launch_fwd_t<64, false, true>(a, stream)
+                     : launch_fwd_t<128, false, true>(a, stream);
 }
 
 }  // namespace fa

@@ -136,6 +136,31 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
                int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Split-KV forward for decode-like shapes: few queries per head (Nq), many
+ * keys (Nk).  Every query attends to all Nk keys (no mask: the new tokens
+ * read the whole cache).  The key tiles are cut into n_splits chunks; each
+ * (head, 128-query tile, chunk) is computed like the forward and leaves its
+ * normalised FP32 partial output and LSE in the workspace, then a merge
+ * kernel combines the chunks with the block merge of "LLM part 06:
+ * FlashAttention - GPU SRAM, tiling and online softmax", section 2:
+ * O = sum_s w_s O_s / sum_s w_s, LSE = m + ln sum_s w_s, w_s = exp(LSE_s - m),
+ * m = max_s LSE_s.  The result equals fa_fwd_gqa with Nq queries and Nk keys,
+ * non-causal, up to rounding.
+ *
+ * q, o : bf16 [B,Hq,Nq,d];  k, v : bf16 [B,Hkv,Nk,d];  lse : float [B,Hq,Nq].
+ * Hkv divides Hq (grouped-query attention; Hkv = Hq for multi-head).
+ * n_splits <= 0 lets the library choose (enough chunks to cover every SM
+ * twice); the count actually used never leaves a chunk empty and is at most
+ * the number of 128-key tiles.
+ * workspace : device buffer of at least
+ *             fa_fwd_splitkv_workspace_bytes(B, Hq, Nq, Nk, d, n_splits)
+ *             bytes, 16-byte aligned, or NULL: the library then allocates and
+ *             frees it on the stream.  Returns 0 for invalid sizes. */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Nq, int Nk, int d, int n_splits);
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int n_splits,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the scratch array built into the library for fa_bwd_noalloc:
  * 8 MiB, i.e. B * H * roundup(N, 128) <= 1048576. */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)

@@ -119,3 +119,30 @@ def test_gqa_head_counts_are_checked_before_launch(fa):
     assert lib.fa_fwd_gqa(*p[:4], 0x10004, 1, 4, 2, 16, 64, 1, 0.125,
                           None) == fa.FA_ERR_MISALIGNED
     assert lib.fa_fwd_gqa(*p, 1, 4, 2, 16, 96, 1, 0.125, None) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_splitkv_argument_checks_before_launch(fa):
+    lib = fa.load()
+    p = [0x10000] * 5
+    ok = [1, 4, 2, 1, 4096, 128, 0.125, 2]      # B, Hq, Hkv, Nq, Nk, d, scale, n_splits
+    def call(args, ws=None, nbytes=0):
+        return lib.fa_fwd_splitkv(*p, *args, ws, nbytes, None)
+    assert call([1, 4, 3, 1, 4096, 128, 0.125, 2]) == fa.FA_ERR_INVALID_ARG   # 3 does not divide 4
+    assert call([1, 4, 2, 0, 4096, 128, 0.125, 2]) == fa.FA_ERR_INVALID_ARG   # Nq = 0
+    assert call([1, 4, 2, 1, 0, 128, 0.125, 2]) == fa.FA_ERR_INVALID_ARG      # Nk = 0
+    assert call([1, 4, 2, 1, 4096, 96, 0.125, 2]) == fa.FA_ERR_UNSUPPORTED    # d = 96
+    assert call(ok, ws=0x10004, nbytes=1 << 30) == fa.FA_ERR_MISALIGNED
+    need = lib.fa_fwd_splitkv_workspace_bytes(1, 4, 1, 4096, 128, 2)
+    assert call(ok, ws=0x10000, nbytes=need - 16) == fa.FA_ERR_NO_MEMORY
+
+
+def test_splitkv_workspace_follows_the_split_plan(fa):
+    lib = fa.load()
+    # 4096 keys = 32 key tiles; 5 requested -> chunks of 7 tiles -> 5 splits;
+    # 40 requested -> one tile per split, 32 splits; per split and query row:
+    # d FP32 outputs + 1 FP32 LSE
+    per = 1 * 4 * 3 * (128 + 1) * 4
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 3, 4096, 128, 5) == 5 * per
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 3, 4096, 128, 40) == 32 * per
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 3, 4096, 128, 1) == per
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 3, 4096, 96, 1) == 0

@@ -46,7 +46,15 @@ CSRC = os.path.join(ROOT, "exact_io_aware_18_gb300", "csrc")
 KERNEL_SRC = {"fwd_bf16": os.path.join(CSRC, "fwd_bf16_sm103.cu"),
               "bwd_dkdv_bf16": os.path.join(CSRC, "bwd_bf16_sm103.cu"),
               "bwd_dq_bf16": os.path.join(CSRC, "bwd_dq_sm103.cu")}
-KERNEL_TRAFFIC = {}
+KERNEL_TRAFFIC = {
+    # profiles/kernels_training_step_b8_h16_n2048_d128_causal.md (ncu --set full)
+    "fwd_bf16": {"bytes": 201413376 + 47730688,
+                 "src_sha256": "7af678f8ad2245719cf3ad560c84fd2e3144f9e92dbe4768de62a93e50853ded"},
+    "bwd_dkdv_bf16": {"bytes": 270609664 + 220932608,
+                      "src_sha256": "3f51b0a700edda43dbaef9206612e923e41c46bf70d24c993827bbdbe5b4102d"},
+    "bwd_dq_bf16": {"bytes": 270613760 + 108294912,
+                    "src_sha256": "d70a5e2d980604d6601114c68ee2c0772662181b6f118c9ae9d4d2f4a630c1f0"},
+}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -156,6 +164,84 @@ def oracle_cores():
 
 
 # ---------------------------------------------------------------- GPU arm
+
+def _timed(torch, stream, fn, iters):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def measure_next_rows(fa, torch, q, k, v, do, stream, iters=20):
+    """Rows beyond the training step, timed after (outside) its timed region on
+    the same seeded inputs.  Grouped-query attention: the training-step shape
+    with 4 query heads per K/V head (K, V: their first H/4 heads)."""
+    scale = fa.default_scale(D)
+    hkv = H // 4
+    kg = k[:, :hkv].contiguous()
+    vg = v[:, :hkv].contiguous()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty(kg.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty_like(dk)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, D) // 4, dtype=torch.float32,
+                     device=q.device)
+    f_fwd, f_bwd = step_flops()
+    fwd_ms = _timed(torch, stream, lambda: fa.fa_fwd_gqa(q, kg, vg, o, lse, CAUSAL, scale,
+                                                           stream), iters)
+    bwd_ms = _timed(torch, stream, lambda: fa.fa_bwd_gqa(q, kg, vg, o, do, lse, dq, dk, dv,
+                                                           CAUSAL, scale, ws, stream), iters)
+    # Split-KV decode: one new query per head against a long cache, grouped
+    # K/V heads.  HBM-bound (K and V are read once); seeded synthetic inputs.
+    db, dhq, dhkv, dnq, dnk = 4, 32, 8, 1, 16384
+    gen = torch.Generator(device=q.device)
+    gen.manual_seed(SEED)
+
+    def rnd(*shape):
+        return torch.randn(*shape, generator=gen, device=q.device).to(torch.bfloat16)
+
+    dq_ = rnd(db, dhq, dnq, D)
+    dk_ = rnd(db, dhkv, dnk, D)
+    dv_ = rnd(db, dhkv, dnk, D)
+    do_ = torch.empty_like(dq_)
+    dlse = torch.empty((db, dhq, dnq), dtype=torch.float32, device=q.device)
+    dws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(db, dhq, dhkv, dnq, dnk, D) // 4 + 4,
+                      dtype=torch.float32, device=q.device)
+    dec_ms = _timed(torch, stream, lambda: fa.fa_fwd_splitkv(dq_, dk_, dv_, do_, dlse, scale, 0,
+                                                              dws, stream), iters)
+    dec_bytes = (2 * db * dhkv * dnk * D * 2 + 2 * db * dhq * dnq * D * 2 + db * dhq * dnq * 4)
+    dec_flops = 4.0 * db * dhq * dnq * dnk * D
+    peaks, _ = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    if fa.fa_device_status(clear=True) != fa.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait in the next-row measurements")
+    return {
+        "splitkv_decode": {
+            "workload": f"B={db} Hq={dhq} Hkv={dhkv} Nq={dnq} Nk={dnk} d={D}, bf16, no mask, "
+                        "library-chosen splits",
+            "algorithmic_bytes_counted": "K and V read once, Q read, O and LSE written",
+            "ms": round(dec_ms, 4),
+            "bound": "hbm",
+            "algorithmic_bytes": dec_bytes,
+            "gbs": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(dec_bytes / (dec_ms * 1e-3) / 1e9 / hbm, 4),
+            "tflops": round(dec_flops / (dec_ms * 1e-3) / 1e12, 2)},
+        "gqa": {"workload": f"B={B} Hq={H} Hkv={hkv} N={N} d={D} causal, bf16",
+                "fwd_ms": round(fwd_ms, 4),
+                "fwd_tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
+                "bwd_ms": round(bwd_ms, 4),
+                "bwd_tflops": round(f_bwd / (bwd_ms * 1e-3) / 1e12, 2),
+                "flops": "4 B Hq N^2 d (causal halved), backward 2.5x"},
+    }
+
 
 def run_gpu(args):
     import torch
@@ -282,6 +368,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     sampler.stop()
+    next_rows = measure_next_rows(fa, torch, q, k, v, do, stream) if rank == 0 else None
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
 
@@ -361,6 +448,7 @@ def run_gpu(args):
                        "tflops": round(kern_flops["bwd_dq_bf16"] / (dq_ms * 1e-3) / 1e12, 2)},
             "bwd_total_tflops": round(f_bwd / ((pre_ms + dkdv_ms + dq_ms) * 1e-3) / 1e12, 2),
         },
+        "next_rows": next_rows,
     }
     print(json.dumps(out), flush=True)
     if world > 1:

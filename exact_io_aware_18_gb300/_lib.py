@@ -47,7 +47,7 @@ _SIGNATURES = {
     "fa_bwd_noalloc": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_fwd_gqa": ([_vp] * 5 + [_i] * 6 + [_f, _vp], _i),
     "fa_bwd_gqa": ([_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp], _i),
-    "fa_fwd_splitkv_workspace_bytes": ([_i] * 6, _sz),
+    "fa_fwd_splitkv_workspace_bytes": ([_i] * 7, _sz),
     "fa_fwd_splitkv": ([_vp] * 5 + [_i] * 6 + [_f, _i, _vp, _sz, _vp], _i),
 }
 
@@ -168,10 +168,10 @@ def fa_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, work
            "fa_bwd_gqa")
 
 
-def fa_fwd_splitkv_workspace_bytes(B: int, Hq: int, Nq: int, Nk: int, d: int,
+def fa_fwd_splitkv_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int,
                                    n_splits: int = 0) -> int:
-    return int(load().fa_fwd_splitkv_workspace_bytes(int(B), int(Hq), int(Nq), int(Nk), int(d),
-                                                     int(n_splits)))
+    return int(load().fa_fwd_splitkv_workspace_bytes(int(B), int(Hq), int(Hkv), int(Nq), int(Nk),
+                                                     int(d), int(n_splits)))
 
 
 def fa_fwd_splitkv(q, k, v, o, lse, scale: float, n_splits: int = 0, workspace=None,

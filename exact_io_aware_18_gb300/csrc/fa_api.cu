@@ -234,22 +234,25 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
              void* stream);
 
 // Split-KV plan: the key tiles are cut into chunks of chunk_tiles; n_splits
-// chunks, none empty.  requested <= 0 asks for enough chunks that the (head,
-// Q tile, chunk) items cover every SM twice.
+// chunks, none empty.  The query rows of a K/V head's group (g query heads x
+// Nq queries, contiguous in memory) form its Q tiles; requested <= 0 asks for
+// enough chunks that the (K/V head, Q tile, chunk) items fill every SM about
+// four times, so that the last partial wave is short.
 struct SplitPlan {
     int n_splits;
     int chunk_tiles;
 };
 
-int split_plan(int B, int Hq, int Nq, int Nk, int requested, SplitPlan* out) {
+int split_plan(int B, int Hq, int Hkv, int Nq, int Nk, int requested, SplitPlan* out) {
     const long long kv_tiles = (static_cast<long long>(Nk) + 127) / 128;
-    const long long q_items = static_cast<long long>(B) * Hq * ((Nq + 127) / 128);
+    const long long group_rows = static_cast<long long>(Hq / Hkv) * Nq;
+    const long long q_items = static_cast<long long>(B) * Hkv * ((group_rows + 127) / 128);
     long long want = requested;
     if (want <= 0) {
         unsigned int* unused;
         int sms = 0;
         if (int rc = work_slot(&unused, &sms)) return rc;
-        want = (2LL * sms + q_items - 1) / q_items;
+        want = (4LL * sms + q_items - 1) / q_items;
     }
     if (want < 1) want = 1;
     if (want > kv_tiles) want = kv_tiles;
@@ -308,10 +311,12 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
     return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, stream);
 }
 
-size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Nq, int Nk, int d, int n_splits) {
+size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                      int n_splits) {
     if (B < 1 || Hq < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
+    if (check_heads(Hq, Hkv) != FA_OK) return 0;
     SplitPlan plan;
-    if (split_plan(B, Hq, Nq, Nk, n_splits, &plan) != FA_OK) return 0;
+    if (split_plan(B, Hq, Hkv, Nq, Nk, n_splits, &plan) != FA_OK) return 0;
     return splitkv_bytes(B, Hq, Nq, d, plan.n_splits);
 }
 
@@ -322,8 +327,10 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
     if (int rc = check_shape(B, Hq, Nq, d, scale)) return rc;
     if (int rc = check_shape(B, Hkv, Nk, d, scale)) return rc;
     if (int rc = check_heads(Hq, Hkv)) return rc;
+    const long long group_rows = static_cast<long long>(Hq / Hkv) * Nq;
+    if (group_rows > (1LL << 30)) return FA_ERR_UNSUPPORTED;
     SplitPlan plan;
-    if (int rc = split_plan(B, Hq, Nq, Nk, n_splits, &plan)) return rc;
+    if (int rc = split_plan(B, Hq, Hkv, Nq, Nk, n_splits, &plan)) return rc;
     const size_t need = splitkv_bytes(B, Hq, Nq, d, plan.n_splits);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void* ws = workspace;
@@ -340,19 +347,24 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
     unsigned int* work;
     int sms;
     CUtensorMap tq, tk, tv;
-    const long long BH = static_cast<long long>(B) * Hq;
     const long long BHkv = static_cast<long long>(B) * Hkv;
+    // The g query heads of a K/V head and their Nq queries are contiguous rows
+    // of q ([B, Hkv, g, Nq, d]), so the kernel sees each K/V head as one
+    // "head" with g * Nq query rows: its Q tiles fill with real rows, and each
+    // K/V tile is read once for the whole group.
+    const int rows = static_cast<int>(group_rows);
     if ((rc = status_ptr(&status)) == FA_OK && (rc = work_slot(&work, &sms)) == FA_OK &&
-        (rc = make_map_bf16(&tq, q, d, Nq, BH)) == FA_OK &&
+        (rc = make_map_bf16(&tq, q, d, rows, BHkv)) == FA_OK &&
         (rc = make_map_bf16(&tk, k, d, Nk, BHkv)) == FA_OK &&
         (rc = make_map_bf16(&tv, v, d, Nk, BHkv)) == FA_OK) {
         // The split kernel stores no O tile: the Q map stands in for O's.
-        fa::FwdArgs a{&tq, &tk, &tv, &tq, nullptr, B, Hq, Nq, d, Hkv, 0,
+        fa::FwdArgs a{&tq, &tk, &tv, &tq, nullptr, B, Hkv, rows, d, Hkv, 0,
                       scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms,
                       Nk, plan.n_splits, plan.chunk_tiles, o_part, lse_part};
         rc = launch_rc(fa::launch_fwd_splitkv_bf16(a, st));
         if (rc == FA_OK) {
-            fa::CombineArgs c{o_part, lse_part, o, lse, static_cast<int>(BH), Nq, d,
+            // Partials and outputs share the row order [B, Hkv, g, Nq] = [B, Hq, Nq].
+            fa::CombineArgs c{o_part, lse_part, o, lse, static_cast<int>(BHkv), rows, d,
                               plan.n_splits};
             rc = launch_rc(fa::launch_splitkv_combine(c, st));
         }

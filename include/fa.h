@@ -149,14 +149,18 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
  *
  * q, o : bf16 [B,Hq,Nq,d];  k, v : bf16 [B,Hkv,Nk,d];  lse : float [B,Hq,Nq].
  * Hkv divides Hq (grouped-query attention; Hkv = Hq for multi-head).
- * n_splits <= 0 lets the library choose (enough chunks to cover every SM
- * twice); the count actually used never leaves a chunk empty and is at most
- * the number of 128-key tiles.
+ * The g = Hq / Hkv query heads of a K/V head share its tiles: their g * Nq
+ * query rows (contiguous in q) are computed together, 128 rows at a time,
+ * so each K/V tile is read once per group.
+ * n_splits <= 0 lets the library choose (enough chunks to fill every SM
+ * about four times); the count actually used never leaves a chunk empty and
+ * is at most the number of 128-key tiles.
  * workspace : device buffer of at least
- *             fa_fwd_splitkv_workspace_bytes(B, Hq, Nq, Nk, d, n_splits)
+ *             fa_fwd_splitkv_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, n_splits)
  *             bytes, 16-byte aligned, or NULL: the library then allocates and
  *             frees it on the stream.  Returns 0 for invalid sizes. */
-size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Nq, int Nk, int d, int n_splits);
+size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                      int n_splits);
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int n_splits,
                    void* workspace, size_t workspace_bytes, void* stream);

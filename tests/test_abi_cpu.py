@@ -132,7 +132,7 @@ def test_splitkv_argument_checks_before_launch(fa):
     assert call([1, 4, 2, 1, 0, 128, 0.125, 2]) == fa.FA_ERR_INVALID_ARG      # Nk = 0
     assert call([1, 4, 2, 1, 4096, 96, 0.125, 2]) == fa.FA_ERR_UNSUPPORTED    # d = 96
     assert call(ok, ws=0x10004, nbytes=1 << 30) == fa.FA_ERR_MISALIGNED
-    need = lib.fa_fwd_splitkv_workspace_bytes(1, 4, 1, 4096, 128, 2)
+    need = lib.fa_fwd_splitkv_workspace_bytes(1, 4, 2, 1, 4096, 128, 2)
     assert call(ok, ws=0x10000, nbytes=need - 16) == fa.FA_ERR_NO_MEMORY
 
 
@@ -142,7 +142,8 @@ def test_splitkv_workspace_follows_the_split_plan(fa):
     # 40 requested -> one tile per split, 32 splits; per split and query row:
     # d FP32 outputs + 1 FP32 LSE
     per = 1 * 4 * 3 * (128 + 1) * 4
-    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 3, 4096, 128, 5) == 5 * per
-    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 3, 4096, 128, 40) == 32 * per
-    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 3, 4096, 128, 1) == per
-    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 3, 4096, 96, 1) == 0
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 2, 3, 4096, 128, 5) == 5 * per
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 2, 3, 4096, 128, 40) == 32 * per
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 4, 3, 4096, 128, 1) == per
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 2, 3, 4096, 96, 1) == 0
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 3, 3, 4096, 128, 1) == 0   # 3 does not divide 4

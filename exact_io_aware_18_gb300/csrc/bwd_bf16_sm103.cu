@@ -7,95 +7,118 @@
 // algorithm", idea 2, recomputation).  Per (b, h), with D_i = dO_i . O_i:
 //   P   = exp(scale S - LSE)      dV = P^T dO        dP = dO V^T
 //   dS  = P o (dP - D)            dK = scale dS^T Q  (dQ: bwd_dq_sm103.cu)
-// One CTA owns one 128-key tile j of one (b, h), keeps K_j and V_j in shared
-// memory and dK_j, dV_j in TMEM, and loops over the 128-row Q tiles i that
-// see those keys (i >= j when causal); the parallelism over key tiles of one
-// head is the sequence parallelism of "FlashAttention-2" (technical
-// architecture, improvement 2).  dQ is left to a second kernel that loops
-// over key tiles per Q tile, so nothing here is reduced across CTAs.
+// A work item is one 128-key tile j of one K/V head: K_j and V_j stay in
+// shared memory and dK_j, dV_j in TMEM while the item loops over the 128-row
+// Q tiles i that see those keys (i >= j when causal) of every query head that
+// reads this K/V head (one head in multi-head attention, the group in
+// grouped-query attention).  The parallelism over key tiles is the sequence
+// parallelism of "FlashAttention-2" (technical architecture, improvement 2);
+// dQ is left to a second kernel, so nothing here is reduced across CTAs.
 //
-// Roles (352 threads, one CTA per SM):
-//   warp 0      TMA producer: K_j, V_j once; per Q tile, into a two-deep ring
+// GB300 mapping: a persistent kernel, one CTA per SM (512 threads), that
+// claims key tiles from a per-launch counter (heavy tiles first, a few heads
+// at a time so that their Q and dO tiles stay in L2).  Items run back to back:
+// the next item's K, V and first [Q | dO] stages load while the current one
+// finishes, and a warpgroup of its own writes the finished dK, dV out of TMEM
+// while the next item computes.
+//   warp 0      TMA producer: K_j, V_j per item (once the last MMAs that read
+//               the previous ones have finished); per Q tile, a two-deep ring
 //               of [Q_i | dO_i] stages plus the 128-entry LSE2 / D vectors.
-//   warps 1, 10 two MMA issuers (one thread each).  A single thread issues a
+//   warps 1, 2  two MMA issuers (one thread each).  A single thread issues a
 //               128 x 128 x 16 tcgen05.mma about as fast as the tensor pipe
-//               runs it, so every barrier check in between would leave the
-//               pipe idle; with two issuers one keeps the pipe fed while the
+//               runs it, so with two issuers one keeps the pipe fed while the
 //               other waits.  Each issuer overwrites only TMEM it alone reads,
 //               after those reads in its own issue order:
 //                 issuer A: dV += P^T_t dO_t (A = P^T in TMEM, after P_FULL),
 //                           then S^T_t+1 = K Q_t+1^T over P^T_t;
 //                 issuer B: dK += dS^T_t Q_t (A = dS^T in TMEM, after DS_FULL),
 //                           then dP^T_t+1 = V dO_t+1^T over dS^T_t.
-//               So S^T and dP^T of the next tile run while the P and dS math
-//               of this one does.  A stage is free once both issuers commit.
-//   warps 2..9  thread (r, h) owns key row r (TMEM lane r) and column half h
-//               (warps 2-5: h = 0, warps 6-9: h = 1).  Phase P: 64 entries of
+//               An item's first dV (dK) MMA, which overwrites the
+//               accumulator, waits until the epilogue warps have read the
+//               previous item's dV (dK) out.
+//   warp 3      claims key tiles (the next one once the producer has issued
+//               the current one's last loads) into a small queue that every
+//               role reads in order.
+//   warps 4-11  thread (r, h) owns key row r (TMEM lane r) and column half h
+//               (warps 4-7: h = 0, warps 8-11: h = 1).  Phase P: 64 entries of
 //               the P^T row = exp2(S^T * scale*log2e - LSE2), kept in
 //               registers and written back as BF16 into the first 32 of its
 //               own 64 S^T columns.  Phase dS: dS^T = P o (dP^T - D), BF16,
 //               likewise into its own dP^T columns (scale is applied to dK
-//               once, when it leaves TMEM).  At the end: dK, dV rows out of
-//               TMEM into swizzled shared-memory boxes, then to global memory
-//               (FP32) by TMA stores of whole 128-byte rows.
+//               once, when it leaves TMEM).
+//   warps 12-15 epilogue: warp w reads rows 32 (w % 4) .. +32 of dV, then of
+//               dK, 32 columns at a time out of TMEM into a 4 KB swizzled
+//               shared-memory box and writes each box by TMA store.  An SM
+//               writes about 30 bytes a cycle, so the 2 x 64 KB of FP32
+//               gradients of an item take thousands of cycles; here they are
+//               written while the next item's tiles run.
+// Warpgroups 0 and 3 hand registers to the math warpgroups 1 and 2.
 // TMEM columns: S^T [0,128) (P^T halves at [0,32) and [64,96)),
 // dP^T [128,256) (dS^T halves at [128,160) and [192,224)), dV [256,256+d),
-// dK [256+d, 256+2d).  Eleven warps cap a thread at 168 registers (the
-// register file is split among the four SM sub-partitions, three warps on
-// three of them).  All waits are bounded (see sm103_primitives.cuh).
+// dK [256+d, 256+2d).  All waits are bounded (see sm103_primitives.cuh).
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kMaxDynSmem = 232448;  // 227 KB opt-in limit per block
+constexpr int kMaxDynSmem = 232448;     // 227 KB opt-in limit per block
+constexpr uint32_t kRegsLight = 64;     // warpgroups 0 and 3 after the split
+constexpr uint32_t kRegsMath = 192;     // warpgroups 1 and 2 after the split
+static_assert(128 * (2 * kRegsLight + 2 * kRegsMath) <= 512 * 128, "register split");
 
 template <int D>
 struct BwdCfg {
     static constexpr int BM = 128;  // query rows per Q tile
-    static constexpr int BN = 128;  // keys per CTA
+    static constexpr int BN = 128;  // keys per item
     static constexpr int KB = D / 64;
     static constexpr int BOX_BYTES = 128 * 64 * 2;      // 128 x 64 bf16
     static constexpr int TILE_BYTES = KB * BOX_BYTES;    // 128 x D bf16
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // [Q | dO]
     static constexpr int NSQ = 2;                        // stage ring depth
+    static constexpr int QUEUE = 4;                      // claimed-item queue depth
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + TILE_BYTES;
     static constexpr int OFF_STAGE = OFF_V + TILE_BYTES;
     static constexpr int OFF_VEC = OFF_STAGE + NSQ * STAGE_BYTES;  // NSQ x (lse2, delta)
-    static constexpr int OFF_BAR = OFF_VEC + NSQ * 1024;
+    static constexpr int OFF_STG = OFF_VEC + NSQ * 1024;           // 4 epilogue boxes of 4 KB
+    static constexpr int OFF_BAR = OFF_STG + 4 * 4096;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int LAYOUT_BYTES = OFF_BAR + BAR_BYTES;
-    static constexpr int SMEM_BYTES =
-        (LAYOUT_BYTES + 1024 <= kMaxDynSmem) ? LAYOUT_BYTES + 1024 : kMaxDynSmem;
-    static_assert(LAYOUT_BYTES <= kMaxDynSmem, "backward tiles do not fit in shared memory");
-    // The epilogue stages FP32 dV and dK (2 x 8 warps x d/64 boxes of 4 KB)
-    // over K, V and the stage ring, which start at offset 0 and are contiguous.
-    static_assert(OFF_K == 0 && 2 * 8 * (D / 64) * 4096 <= OFF_VEC,
-                  "dK/dV staging does not fit over the tiles");
+    static constexpr int OFF_ITEMS = OFF_BAR + BAR_BYTES;
+    static constexpr int LAYOUT_BYTES = OFF_ITEMS + QUEUE * 4;
+    static constexpr int SMEM_BYTES = LAYOUT_BYTES + 1024;  // + alignment slack
+    static_assert(SMEM_BYTES <= kMaxDynSmem, "backward tiles do not fit in shared memory");
+    static_assert(OFF_STG % 1024 == 0, "swizzled staging boxes need 1024-byte alignment");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
-    static constexpr int THREADS = 352;
+    static constexpr int THREADS = 512;
     static constexpr int COMPUTE_WARPS = 8;
+    // Arrivals on ITEM_EMPTY: producer, two issuers, 8 math and 4 epilogue warps.
+    static constexpr int ITEM_READERS = 15;
 };
 
-template <int NSQ>
+template <int NSQ, int QUEUE>
 struct BwdBars {
     static constexpr int KV_FULL = 0;
-    static constexpr int Q_FULL = 1;
+    static constexpr int KV_EMPTY = KV_FULL + 1;
+    static constexpr int Q_FULL = KV_EMPTY + 1;
     static constexpr int Q_EMPTY = Q_FULL + NSQ;
     static constexpr int S_FULL = Q_EMPTY + NSQ;
     static constexpr int DP_FULL = S_FULL + 1;
     static constexpr int P_FULL = DP_FULL + 1;
     static constexpr int DS_FULL = P_FULL + 1;
     static constexpr int ACC_FULL = DS_FULL + 1;
-    static constexpr int DONE = ACC_FULL + 1;
+    static constexpr int DV_FREE = ACC_FULL + 1;
+    static constexpr int DK_FREE = DV_FREE + 1;
+    static constexpr int ITEM_FULL = DK_FREE + 1;  // QUEUE
+    static constexpr int ITEM_EMPTY = ITEM_FULL + QUEUE;
+    static constexpr int CLAIM_OK = ITEM_EMPTY + QUEUE;
+    static constexpr int DONE = CLAIM_OK + 1;
     static constexpr int COUNT = DONE + 1;
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(512, 1)
     bwd_dkdv_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
@@ -105,9 +128,10 @@ __global__ void __launch_bounds__(352, 1)
                          const float* __restrict__ delta, const float* __restrict__ lse2,
                          int N, int n_pad, int BHkv, int Hkv, int n_rep, int n_tiles,
                          int group, float scale, float scale_log2, unsigned int* status,
-                         unsigned long long timeout_ns) {
+                         unsigned long long timeout_ns, unsigned int* work) {
     using C = BwdCfg<D>;
-    using Bar = BwdBars<C::NSQ>;
+    using Bar = BwdBars<C::NSQ, C::QUEUE>;
+    static_assert(8 * Bar::COUNT + 8 <= C::BAR_BYTES, "barrier area");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     if (smem + C::LAYOUT_BYTES > smem_raw + C::SMEM_BYTES) {
@@ -127,28 +151,34 @@ __global__ void __launch_bounds__(352, 1)
     auto do_of = [&](int st) -> uint32_t { return s_stage + st * C::STAGE_BYTES + C::TILE_BYTES; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * Bar::COUNT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* items = reinterpret_cast<volatile int*>(smem + C::OFF_ITEMS);
+    const int n_items = BHkv * n_tiles;
 
-    // Key tile 0 sees every Q tile under a causal mask: heavy tiles first,
-    // a few heads at a time so their Q and dO stay in L2.
-    const long long lin = blockIdx.x + static_cast<long long>(gridDim.x) *
-                                           (blockIdx.y + static_cast<long long>(gridDim.y) *
-                                                             blockIdx.z);
-    const TileHead th = grouped_order(lin, BHkv, n_tiles, group, false);
-    const int kt = th.tile;
-    const int bkv = th.head;  // K/V head (b * Hkv + j)
-    const int i0 = CAUSAL ? kt : 0;
-    const int n_q = n_tiles - i0;
-    // Step t covers query head r = t / n_q of this K/V head's group (the
-    // n_rep query heads b * Hq + j * n_rep + r, Hq = n_rep * Hkv) and its Q
-    // tile i = i0 + t % n_q; with n_rep = 1 this is plain multi-head attention.
-    const int n_steps = n_rep * n_q;
-    const int bhq0 = (bkv / Hkv) * (Hkv * n_rep) + (bkv % Hkv) * n_rep;
+    // Item: key tile kt of K/V head bkv (key tile 0 sees every Q tile under a
+    // causal mask: heavy tiles first, a few heads at a time).  Step t of an
+    // item covers query head bhq0 + t / n_q of the K/V head's group (Hq =
+    // n_rep * Hkv) and its Q tile i0 + t % n_q.
+    struct Work {
+        int kt, bkv, i0, n_q, n_steps, bhq0;
+    };
+    auto work_of = [&](int item) -> Work {
+        const TileHead th = grouped_order(item, BHkv, n_tiles, group, false);
+        Work w;
+        w.kt = th.tile;
+        w.bkv = th.head;
+        w.i0 = CAUSAL ? w.kt : 0;
+        w.n_q = n_tiles - w.i0;
+        w.n_steps = n_rep * w.n_q;
+        w.bhq0 = (w.bkv / Hkv) * (Hkv * n_rep) + (w.bkv % Hkv) * n_rep;
+        return w;
+    };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(Bar::KV_FULL), 1);
+        mbar_init(bar(Bar::KV_EMPTY), 2);  // one commit per issuer
         for (int s = 0; s < C::NSQ; ++s) {
             mbar_init(bar(Bar::Q_FULL + s), 1);
             mbar_init(bar(Bar::Q_EMPTY + s), 2);  // one commit per issuer
@@ -158,6 +188,13 @@ __global__ void __launch_bounds__(352, 1)
         mbar_init(bar(Bar::P_FULL), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::DS_FULL), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::ACC_FULL), 2);
+        mbar_init(bar(Bar::DV_FREE), 4);  // one arrival per epilogue warp
+        mbar_init(bar(Bar::DK_FREE), 4);
+        for (int i = 0; i < C::QUEUE; ++i) {
+            mbar_init(bar(Bar::ITEM_FULL + i), 1);
+            mbar_init(bar(Bar::ITEM_EMPTY + i), C::ITEM_READERS);
+        }
+        mbar_init(bar(Bar::CLAIM_OK), 1);
         mbar_init(bar(Bar::DONE), 2);
         *abort_flag = 0;
         mbar_fence_init();
@@ -165,6 +202,8 @@ __global__ void __launch_bounds__(352, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_do);
+        prefetch_tensormap(&tm_dk);
+        prefetch_tensormap(&tm_dv);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -176,206 +215,310 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const WaitCtx wc{status, timeout_ns, abort_flag};
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            auto load_tile = [&](int t) {
-                const int st = t % C::NSQ;
-                const int i = i0 + t % n_q;
-                const int bh = bhq0 + t / n_q;  // query head
-                const uint32_t fb = bar(Bar::Q_FULL + st);
-                mbar_arrive_expect_tx(fb, C::STAGE_BYTES + 1024);
-                for (int kb = 0; kb < C::KB; ++kb) {
-                    tma_load_3d(q_of(st) + kb * C::BOX_BYTES, &tm_q, fb, kb * 64, i * C::BM, bh);
-                    tma_load_3d(do_of(st) + kb * C::BOX_BYTES, &tm_do, fb, kb * 64, i * C::BM,
-                                bh);
+    // Item k of this CTA from the queue (single-thread roles); -1 at the end
+    // of the work or when a wait gave up.
+    auto take_item = [&](int k) -> int {
+        const int slot = k % C::QUEUE;
+        if (!mbar_wait(bar(Bar::ITEM_FULL + slot), (k / C::QUEUE) & 1, wc)) return -1;
+        const int item = items[slot];
+        mbar_arrive(bar(Bar::ITEM_EMPTY + slot));
+        return item;
+    };
+    // The same for a whole warp: every lane waits and reads, lane 0 arrives.
+    auto take_item_warp = [&](int k) -> int {
+        const int slot = k % C::QUEUE;
+        const bool ok = __all_sync(
+            0xffffffffu, mbar_wait(bar(Bar::ITEM_FULL + slot), (k / C::QUEUE) & 1, wc));
+        const int item = ok ? items[slot] : -1;
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(bar(Bar::ITEM_EMPTY + slot));
+        return item;
+    };
+
+    if (warp < 4 || warp >= 12) {
+        regs_decrease<kRegsLight>();
+        if (warp == 3) {
+            // ------------------------------------------------------------ claimer
+            if (lane == 0) {
+                bool ok = true, claimed_last = false;
+                for (int k = 0; ok; ++k) {
+                    const int slot = k % C::QUEUE;
+                    if (k >= 1) ok = mbar_wait(bar(Bar::CLAIM_OK), (k - 1) & 1, wc);
+                    if (ok && k >= C::QUEUE)
+                        ok = mbar_wait(bar(Bar::ITEM_EMPTY + slot), ((k / C::QUEUE) - 1) & 1, wc);
+                    if (!ok) break;
+                    int item = static_cast<int>(blockIdx.x);
+                    if (k > 0) {
+                        const unsigned int t = atomicAdd(work, 1u);
+                        item = static_cast<int>(gridDim.x + t);
+                        if (item >= n_items) {
+                            claimed_last = true;
+                            // Every CTA ends with exactly one failed claim; the one
+                            // that draws the last number resets the counter.
+                            if (t == static_cast<unsigned int>(n_items) - 1u) atomicExch(work, 0u);
+                        }
+                    }
+                    if (item >= n_items) item = -1;
+                    items[slot] = item;
+                    mbar_arrive(bar(Bar::ITEM_FULL + slot));
+                    if (item < 0) break;
                 }
-                const long long voff = static_cast<long long>(bh) * n_pad + i * C::BM;
-                bulk_load(s_vec + st * 1024, lse2 + voff, 512, fb);
-                bulk_load(s_vec + st * 1024 + 512, delta + voff, 512, fb);
-            };
-            mbar_arrive_expect_tx(bar(Bar::KV_FULL), 2 * C::TILE_BYTES);
-            for (int kb = 0; kb < C::KB; ++kb) {
-                tma_load_3d(s_k + kb * C::BOX_BYTES, &tm_k, bar(Bar::KV_FULL), kb * 64,
-                            kt * C::BN, bkv);
-                tma_load_3d(s_v + kb * C::BOX_BYTES, &tm_v, bar(Bar::KV_FULL), kb * 64,
-                            kt * C::BN, bkv);
+                while (!claimed_last) {  // after giving up: finish drawing as normal
+                    const unsigned int t = atomicAdd(work, 1u);
+                    if (gridDim.x + t >= static_cast<unsigned int>(n_items)) {
+                        claimed_last = true;
+                        if (t == static_cast<unsigned int>(n_items) - 1u) atomicExch(work, 0u);
+                    }
+                }
             }
-            int issued = 0;
-            for (; issued < n_steps; ++issued) {
-                const int use = issued / C::NSQ;
-                if (use > 0 &&
-                    !mbar_wait(bar(Bar::Q_EMPTY + issued % C::NSQ), (use - 1) & 1, wc))
-                    break;
-                load_tile(issued);
+            __syncwarp();
+        } else if (warp == 0) {
+            // ------------------------------------------------------------ producer
+            if (lane == 0) {
+                int g = 0, issued = 0, kv_loads = 0;
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int item = take_item(k);
+                    if (item < 0) break;
+                    const Work w = work_of(item);
+                    // K, V of this item once the last MMAs that read the previous
+                    // item's have finished.
+                    if (k >= 1) ok = mbar_wait(bar(Bar::KV_EMPTY), (k - 1) & 1, wc);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(Bar::KV_FULL), 2 * C::TILE_BYTES);
+                    for (int kb = 0; kb < C::KB; ++kb) {
+                        tma_load_3d(s_k + kb * C::BOX_BYTES, &tm_k, bar(Bar::KV_FULL), kb * 64,
+                                    w.kt * C::BN, w.bkv);
+                        tma_load_3d(s_v + kb * C::BOX_BYTES, &tm_v, bar(Bar::KV_FULL), kb * 64,
+                                    w.kt * C::BN, w.bkv);
+                    }
+                    kv_loads = k + 1;
+                    for (int t = 0; t < w.n_steps && ok; ++t, ++g) {
+                        const int st = g % C::NSQ;
+                        const int use = g / C::NSQ;
+                        if (use > 0) ok = mbar_wait(bar(Bar::Q_EMPTY + st), (use - 1) & 1, wc);
+                        if (!ok) break;
+                        const int i = w.i0 + t % w.n_q;
+                        const int bh = w.bhq0 + t / w.n_q;  // query head
+                        const uint32_t fb = bar(Bar::Q_FULL + st);
+                        mbar_arrive_expect_tx(fb, C::STAGE_BYTES + 1024);
+                        for (int kb = 0; kb < C::KB; ++kb) {
+                            tma_load_3d(q_of(st) + kb * C::BOX_BYTES, &tm_q, fb, kb * 64,
+                                        i * C::BM, bh);
+                            tma_load_3d(do_of(st) + kb * C::BOX_BYTES, &tm_do, fb, kb * 64,
+                                        i * C::BM, bh);
+                        }
+                        const long long voff = static_cast<long long>(bh) * n_pad + i * C::BM;
+                        bulk_load(s_vec + st * 1024, lse2 + voff, 512, fb);
+                        bulk_load(s_vec + st * 1024 + 512, delta + voff, 512, fb);
+                        issued = g + 1;
+                    }
+                    if (ok) mbar_arrive(bar(Bar::CLAIM_OK));  // the next item may be claimed
+                }
+                // Drain: no copy may still be landing when the CTA exits.
+                if (kv_loads > 0)
+                    mbar_wait_drain(bar(Bar::KV_FULL), (kv_loads - 1) & 1, timeout_ns);
+                for (int t = (issued > C::NSQ ? issued - C::NSQ : 0); t < issued; ++t)
+                    mbar_wait_drain(bar(Bar::Q_FULL + t % C::NSQ), (t / C::NSQ) & 1, timeout_ns);
             }
-            mbar_wait_drain(bar(Bar::KV_FULL), 0, timeout_ns);
-            for (int t = (issued > C::NSQ ? issued - C::NSQ : 0); t < issued; ++t)
-                mbar_wait_drain(bar(Bar::Q_FULL + t % C::NSQ), (t / C::NSQ) & 1, timeout_ns);
-        }
-    } else if (warp == 1 || warp == 10) {
-        // ------------------------------------------------------------ MMA issuers
-        if (lane == 0) {
-            constexpr uint32_t id_sp = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
-            constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);    // dV, dK: B MN-major
-            const bool issuer_a = (warp == 1);
-            // Base descriptors; each MMA below only moves the start address.
-            const uint64_t d_k = smem_desc_sw128(s_k, 16, 1024);                // A of S^T
-            const uint64_t d_v = smem_desc_sw128(s_v, 16, 1024);                // A of dP^T
-            // Stage 0 descriptors; stage st sits st * STAGE_BYTES further on.
-            // issuer A: Q (K-major, B of S^T) and dO (MN-major, B of dV);
-            // issuer B: dO (K-major, B of dP^T) and Q (MN-major, B of dK).
-            const uint64_t d_kmaj0 = smem_desc_sw128(issuer_a ? q_of(0) : do_of(0), 16, 1024);
-            const uint64_t d_mn0 = smem_desc_sw128(issuer_a ? do_of(0) : q_of(0), C::BOX_BYTES, 1024);
-            const uint64_t d_first = issuer_a ? d_k : d_v;
-            const uint32_t c_first = issuer_a ? C::COL_S : C::COL_DP;   // S^T or dP^T
-            const uint32_t c_acc = issuer_a ? C::COL_DV : C::COL_DK;    // dV or dK
-            const uint32_t c_a = issuer_a ? C::COL_S : C::COL_DP;       // P^T or dS^T
-            const int ready_bar = issuer_a ? Bar::P_FULL : Bar::DS_FULL;
-            const int full_bar = issuer_a ? Bar::S_FULL : Bar::DP_FULL;
-            // First GEMM of tile t: S^T_t = K Q_t^T (A) or dP^T_t = V dO_t^T (B).
-            auto issue_first = [&](int t) -> bool {
-                const int st = t % C::NSQ;
-                if (!mbar_wait(bar(Bar::Q_FULL + st), (t / C::NSQ) & 1, wc)) return false;
-                tc_fence_after();
+            __syncwarp();
+        } else if (warp == 1 || warp == 2) {
+            // ------------------------------------------------------------ MMA issuers
+            if (lane == 0) {
+                constexpr uint32_t id_sp = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
+                constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);    // dV, dK: B MN-major
+                const bool issuer_a = (warp == 1);
+                // Base descriptors; each MMA below only moves the start address.
+                const uint64_t d_k = smem_desc_sw128(s_k, 16, 1024);  // A of S^T
+                const uint64_t d_v = smem_desc_sw128(s_v, 16, 1024);  // A of dP^T
+                // Stage 0 descriptors; stage st sits st * STAGE_BYTES further on.
+                // issuer A: Q (K-major, B of S^T) and dO (MN-major, B of dV);
+                // issuer B: dO (K-major, B of dP^T) and Q (MN-major, B of dK).
+                const uint64_t d_kmaj0 = smem_desc_sw128(issuer_a ? q_of(0) : do_of(0), 16, 1024);
+                const uint64_t d_mn0 =
+                    smem_desc_sw128(issuer_a ? do_of(0) : q_of(0), C::BOX_BYTES, 1024);
+                const uint64_t d_first = issuer_a ? d_k : d_v;
+                const uint32_t c_first = issuer_a ? C::COL_S : C::COL_DP;  // S^T or dP^T
+                const uint32_t c_acc = issuer_a ? C::COL_DV : C::COL_DK;   // dV or dK
+                const uint32_t c_a = issuer_a ? C::COL_S : C::COL_DP;      // P^T or dS^T
+                const int ready_bar = issuer_a ? Bar::P_FULL : Bar::DS_FULL;
+                const int full_bar = issuer_a ? Bar::S_FULL : Bar::DP_FULL;
+                const int free_bar = issuer_a ? Bar::DV_FREE : Bar::DK_FREE;
+                // First GEMM of step g: S^T = K Q^T (A) or dP^T = V dO^T (B).
+                auto issue_first = [&](int g) -> bool {
+                    const int st = g % C::NSQ;
+                    if (!mbar_wait(bar(Bar::Q_FULL + st), (g / C::NSQ) & 1, wc)) return false;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                    mma_ss(tmem + c_first, desc_advance(d_first, koff),
-                           desc_advance(d_kmaj0, st * C::STAGE_BYTES + koff), id_sp, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                        mma_ss(tmem + c_first, desc_advance(d_first, koff),
+                               desc_advance(d_kmaj0, st * C::STAGE_BYTES + koff), id_sp, kk > 0);
+                    }
+                    tc_commit(bar(full_bar));
+                    return true;
+                };
+                int g = 0;  // step counter across this CTA's items
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int item = take_item(k);
+                    if (item < 0) break;
+                    const Work w = work_of(item);
+                    ok = mbar_wait(bar(Bar::KV_FULL), k & 1, wc) && issue_first(g);
+                    // K (V) is read for the last time by the item's last first GEMM.
+                    if (ok && w.n_steps == 1) tc_commit(bar(Bar::KV_EMPTY));
+                    for (int t = 0; t < w.n_steps && ok; ++t, ++g) {
+                        const int st = g % C::NSQ;
+                        ok = mbar_wait(bar(ready_bar), g & 1, wc);
+                        // The item's first accumulation overwrites dV (dK): the
+                        // epilogue must have read the previous item's out.
+                        if (ok && t == 0 && k >= 1) ok = mbar_wait(bar(free_bar), (k - 1) & 1, wc);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // dV += P^T dO (A) or dK += dS^T Q (B); the BF16 halves of
+                        // P^T / dS^T (queries 0-63, 64-127) sit at columns [0,32)
+                        // and [64,96) of their fp32 region.
+#pragma unroll
+                        for (int kk = 0; kk < C::BM / 16; ++kk) {
+                            const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                            mma_ts(tmem + c_acc, tmem + c_a + acol,
+                                   desc_advance(d_mn0, st * C::STAGE_BYTES + kk * 2048), id_kv,
+                                   (t > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(bar(Bar::Q_EMPTY + st));  // this issuer no longer reads stage g
+                        if (t + 1 < w.n_steps) {
+                            ok = issue_first(g + 1);
+                            if (ok && t + 2 == w.n_steps) tc_commit(bar(Bar::KV_EMPTY));
+                        }
+                    }
+                    if (ok) tc_commit(bar(Bar::ACC_FULL));
                 }
-                tc_commit(bar(full_bar));
-                return true;
-            };
-            bool ok = mbar_wait(bar(Bar::KV_FULL), 0, wc) && issue_first(0);
-            for (int t = 0; t < n_steps && ok; ++t) {
-                const int st = t % C::NSQ;
-                ok = mbar_wait(bar(ready_bar), t & 1, wc);
+            }
+            __syncwarp();
+        } else {
+            // ------------------------------------------------------------ epilogue
+            // Warp e (of warps 12-15) owns TMEM lanes 32 (e % 4) .. +32: rows
+            // of dV, then of dK, 32 columns (one 4 KB box) at a time.
+            const int wq = warp & 3;
+            const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+            const uint32_t box = s_base + C::OFF_STG + static_cast<uint32_t>(wq * 4096);
+            constexpr int NCH = D / 32;  // 32-column chunks of dV (and of dK)
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int item = take_item_warp(k);
+                if (item < 0) break;
+                const Work w = work_of(item);
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::ACC_FULL), k & 1, wc));
                 if (!ok) break;
                 tc_fence_after();
-                // dV += P^T_t dO_t (A) or dK += dS^T_t Q_t (B); the BF16 halves
-                // of P^T / dS^T (queries 0-63, 64-127) sit at columns [0,32) and
-                // [64,96) of their fp32 region.
-#pragma unroll
-                for (int kk = 0; kk < C::BM / 16; ++kk) {
-                    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-                    mma_ts(tmem + c_acc, tmem + c_a + acol, desc_advance(d_mn0, st * C::STAGE_BYTES + kk * 2048),
-                           id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+                const int row0 = w.kt * C::BN + wq * 32;
+#pragma unroll 1
+                for (int c = 0; c < 2 * NCH; ++c) {
+                    uint32_t a[32];
+                    tmem_ld32(t_lane + C::COL_DV + 32 * c, a);  // dK follows dV
+                    if (c == NCH - 1 || c == 2 * NCH - 1) {
+                        // This warp has read its rows of dV (dK) out.
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(c == NCH - 1 ? Bar::DV_FREE : Bar::DK_FREE));
+                    }
+                    if (lane == 0) bulk_wait_read_all();  // the box is free again
+                    __syncwarp();
+                    st_row_sw128_f32(box, lane, a, c < NCH ? 1.f : scale);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < N) {
+                        tma_store_3d(c < NCH ? &tm_dv : &tm_dk, box, 32 * (c % NCH), row0, w.bkv);
+                        bulk_commit();
+                    }
                 }
-                tc_commit(bar(Bar::Q_EMPTY + st));  // this issuer no longer reads stage t
-                if (t + 1 < n_steps) ok = issue_first(t + 1);
             }
-            if (ok) tc_commit(bar(Bar::ACC_FULL));
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        regs_increase<kRegsMath>();
         // ------------------------------------------------------------ P / dS
         const int wq = warp & 3;
-        const int h = (warp - 2) >> 2;       // column half
+        const int h = (warp - 4) >> 2;       // column half
         const int r = wq * 32 + lane;        // key row
-        const int kglob = kt * C::BN + r;    // key index inside the head
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const float* vec_base = reinterpret_cast<const float*>(smem + C::OFF_VEC);
-        const bool key_pad = kglob >= N;
+        int g = 0;  // step counter across this CTA's items
         bool ok = true;
-        for (int t = 0; t < n_steps; ++t) {
-            const int st = t % C::NSQ;
-            const int i = i0 + t % n_q;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_FULL), t & 1, wc) &&
-                                             mbar_wait(bar(Bar::Q_FULL + st),
-                                                       (t / C::NSQ) & 1, wc));
-            if (!ok) break;
-            tc_fence_after();
-            const float* l2v = vec_base + st * 256 + 64 * h;
-            const float* dlt = vec_base + st * 256 + 128 + 64 * h;
-            // Phase P: entries [64h, 64h+64) of this key's row of P^T.
-            float p[64];
-            {
-                uint32_t sr[64];
-                tmem_ld64(t_lane + C::COL_S + 64 * h, sr);
-                const int q0 = i * C::BM + 64 * h;  // query index of entry 0
-                if (key_pad || (CAUSAL && i == kt)) {
+        for (int k = 0; ok; ++k) {
+            const int item = take_item_warp(k);
+            if (item < 0) break;
+            const Work w = work_of(item);
+            const int kglob = w.kt * C::BN + r;  // key index inside the head
+            const bool key_pad = kglob >= N;
+            for (int t = 0; t < w.n_steps; ++t, ++g) {
+                const int st = g % C::NSQ;
+                const int i = w.i0 + t % w.n_q;
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_FULL), g & 1, wc) &&
+                                                 mbar_wait(bar(Bar::Q_FULL + st),
+                                                           (g / C::NSQ) & 1, wc));
+                if (!ok) break;
+                tc_fence_after();
+                const float* l2v = vec_base + st * 256 + 64 * h;
+                const float* dlt = vec_base + st * 256 + 128 + 64 * h;
+                // Phase P: entries [64h, 64h+64) of this key's row of P^T.
+                float p[64];
+                {
+                    uint32_t sr[64];
+                    tmem_ld64(t_lane + C::COL_S + 64 * h, sr);
+                    const int q0 = i * C::BM + 64 * h;  // query index of entry 0
+                    if (key_pad || (CAUSAL && i == w.kt)) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const float x =
-                            ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, -l2v[c]));
-                        p[c] = (key_pad || q0 + c < kglob) ? 0.f : x;
+                        for (int c = 0; c < 64; ++c) {
+                            const float x =
+                                ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, -l2v[c]));
+                            p[c] = (key_pad || q0 + c < kglob) ? 0.f : x;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, -l2v[c]));
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, -l2v[c]));
                 }
-            }
-            {
-                uint32_t pk[32];
+                {
+                    uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
-                tmem_st32(t_lane + C::COL_S + 64 * h, pk);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Bar::P_FULL));
+                    for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+                    tmem_st32(t_lane + C::COL_S + 64 * h, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(Bar::P_FULL));
 
-            // Phase dS: dS^T = P o (dP^T - D) * scale, BF16, over its dP^T columns.
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DP_FULL), t & 1, wc));
-            if (!ok) break;
-            tc_fence_after();
-            {
-                uint32_t dr[64];
-                tmem_ld64(t_lane + C::COL_DP + 64 * h, dr);
-                uint32_t w[32];
+                // Phase dS: dS^T = P o (dP^T - D), BF16, over its dP^T columns.
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DP_FULL), g & 1, wc));
+                if (!ok) break;
+                tc_fence_after();
+                {
+                    uint32_t dr[64];
+                    tmem_ld64(t_lane + C::COL_DP + 64 * h, dr);
+                    uint32_t wv[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int c = 2 * e;
-                    w[e] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - dlt[c]),
-                                       p[c + 1] * (__uint_as_float(dr[c + 1]) - dlt[c + 1]));
+                    for (int e = 0; e < 32; ++e) {
+                        const int c = 2 * e;
+                        wv[e] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - dlt[c]),
+                                            p[c + 1] * (__uint_as_float(dr[c + 1]) - dlt[c + 1]));
+                    }
+                    tmem_st32(t_lane + C::COL_DP + 64 * h, wv);
                 }
-                tmem_st32(t_lane + C::COL_DP + 64 * h, w);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(Bar::DS_FULL));
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Bar::DS_FULL));
-        }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::ACC_FULL), 0, wc));
-        if (ok) {
-            // Every MMA has completed, so K, V and the [Q | dO] ring hold the
-            // staging boxes: this warp's 32 rows x d/2 columns of dV, then of
-            // dK, as d/64 boxes of 32 x 32 each, stored by TMA in whole
-            // 128-byte rows.
-            tc_fence_after();
-            constexpr uint32_t kHalfBytes = 8 * (D / 64) * 4096;  // all of dV
-            const uint32_t stg = s_k + static_cast<uint32_t>((warp - 2) * (D / 64) * 4096);
-#pragma unroll
-            for (int ch = 0; ch < D / 64; ++ch) {
-                uint32_t a[32];
-                tmem_ld32(t_lane + C::COL_DV + (D / 2) * h + ch * 32, a);
-                st_row_sw128_f32(stg + ch * 4096, lane, a, 1.f);
-                tmem_ld32(t_lane + C::COL_DK + (D / 2) * h + ch * 32, a);
-                st_row_sw128_f32(stg + kHalfBytes + ch * 4096, lane, a, scale);
-            }
-            fence_async_smem();
-            __syncwarp();
-            const int row0 = kt * C::BN + wq * 32;
-            if (lane == 0 && row0 < N) {
-#pragma unroll
-                for (int ch = 0; ch < D / 64; ++ch) {
-                    tma_store_3d(&tm_dv, stg + ch * 4096, (D / 2) * h + ch * 32, row0, bkv);
-                    tma_store_3d(&tm_dk, stg + kHalfBytes + ch * 4096, (D / 2) * h + ch * 32,
-                                 row0, bkv);
-                }
-                bulk_commit();
-                bulk_wait_read_all();  // the boxes stay in place until read
-            }
-            __syncwarp();
         }
     }
 
     // ---------------------------------------------------------------- teardown
     __syncthreads();
-    if (warp == 10 && lane == 0) tc_commit(bar(Bar::DONE));
+    if (warp == 2 && lane == 0) tc_commit(bar(Bar::DONE));
     if (warp == 1) {
         if (lane == 0) {
             tc_commit(bar(Bar::DONE));  // both issuers' MMAs have completed
@@ -395,14 +538,15 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_tiles = (a.N + C::BN - 1) / C::BN;
-    // Enough heads per group that a group fills about one wave of CTAs.
+    // Enough heads per group that a group fills about one wave of items.
     int group = 128 / n_tiles;
     if (group < 1) group = 1;
-    dim3 grid(n_tiles, a.Hkv, a.B);  // one CTA per key tile of each K/V head
+    const long long n_items = static_cast<long long>(a.B) * a.Hkv * n_tiles;
+    const int grid = static_cast<int>(n_items < a.num_sms ? n_items : a.num_sms);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
         *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dk, *a.tm_dv, a.delta, a.lse2, a.N, a.n_pad,
         a.B * a.Hkv, a.Hkv, a.H / a.Hkv, n_tiles, group, a.scale, a.scale_log2, a.status,
-        a.timeout_ns);
+        a.timeout_ns, a.work);
     return cudaGetLastError();
 }
 

@@ -200,9 +200,12 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* do_,
     if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
     if (int rc = make_map_f32_out(&tdk, dk, d, N, BHkv)) return rc;
     if (int rc = make_map_f32_out(&tdv, dv, d, N, BHkv)) return rc;
+    unsigned int* work;
+    int sms;
+    if (int rc = work_slot(&work, &sms)) return rc;
     fa::BwdArgs a{&tq, &tk, &tv, &tdo, &tdk, &tdv, delta_ws, lse2_ws, B, Hq, N, d,
                   static_cast<int>(n_pad_of(N)), Hkv, causal ? 1 : 0, scale,
-                  scale * 1.4426950408889634f, status, g_timeout_ns.load()};
+                  scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms};
     return launch_rc(fa::launch_bwd_dkdv_bf16(a, static_cast<cudaStream_t>(stream)));
 }
 

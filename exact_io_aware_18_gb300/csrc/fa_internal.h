@@ -84,6 +84,8 @@ struct BwdArgs {
     float scale_log2;  // scale * log2(e), for recomputing P
     unsigned int* status;
     unsigned long long timeout_ns;
+    unsigned int* work;  // tile counter of this launch, zero between launches
+    int num_sms;         // persistent grid size
 };
 
 cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t stream);

@@ -73,7 +73,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        // Test the phase several times between reads of the timer and the
+        // abort flag: a waiter that checks them after every test notices
+        // the phase about twice as late (about 250 against 130 cycles).
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (*w.abort_flag) return false;
         if (global_timer_ns() - t0 > w.timeout_ns) {
             *w.abort_flag = 1;
@@ -91,7 +96,9 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > timeout_ns) return false;
     }
 }

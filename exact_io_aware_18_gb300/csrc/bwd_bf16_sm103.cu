@@ -373,6 +373,13 @@ __global__ void __launch_bounds__(512, 1)
                         // The item's first accumulation overwrites dV (dK): the
                         // epilogue must have read the previous item's out.
                         if (ok && t == 0 && k >= 1) ok = mbar_wait(bar(free_bar), (k - 1) & 1, wc);
+                        // Issuer B holds dK_t and dP^T_t+1 until issuer A's S^T_t+1 is
+                        // done: A's dV_t, S^T_t+1 lead to the next P phase and should
+                        // not share the pipe; B's pair then runs during that P phase.
+                        // S_FULL cannot pass step t+1 before this wait: S^T_t+2 needs
+                        // the stage that B frees only after dK_t.
+                        if (ok && !issuer_a && t + 1 < w.n_steps)
+                            ok = mbar_wait(bar(Bar::S_FULL), (g + 1) & 1, wc);
                         if (!ok) break;
                         tc_fence_after();
                         // dV += P^T dO (A) or dK += dS^T Q (B); the BF16 halves of

@@ -112,3 +112,10 @@ def attention_inputs(seed: int, B: int, H: int, N: int, d: int, dtype: str = "bf
         else:
             out[name] = z
     return out
+
+
+def random_signs(seed: int, d: int) -> np.ndarray:
+    """d random signs (+1.0 / -1.0, float32): entry i is -1 when bit 63 of word
+    i of the splitmix64 stream of ``seed`` is set."""
+    w = splitmix64_words(seed, 0, d)
+    return np.where((w >> np.uint64(63)) == 1, np.float32(-1.0), np.float32(1.0)).astype(np.float32)

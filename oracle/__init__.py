@@ -201,3 +201,104 @@ def attention_bwd_gqa(q, k, v, do, causal: bool, scale: float, o_storage="exact"
     dk = dk.reshape(B, Hkv, g, N, d).sum(axis=2)
     dv = dv.reshape(B, Hkv, g, N, d).sum(axis=2)
     return dq.reshape(B, Hq, N, d), dk, dv, dvec.reshape(B, Hq, N)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) with incoherent processing
+#
+# "FlashAttention scaling, multi-GPU training and weight quantization"
+# (section 1, FlashAttention-3, FP8 low-precision support) names two devices
+# that keep FP8 attention accurate: block quantisation, where each small tile
+# gets a scale of its own, and incoherent processing, where Q and K are
+# multiplied by a random orthogonal matrix before quantisation so that outlier
+# channels are spread over all channels.  The pages fix neither the matrix,
+# the tile, the scale rule nor which operands go to FP8; the readings taken
+# here: the matrix is a Hadamard transform with random signs (orthogonal, and
+# applied in O(d log d)); a tile is 128 rows of one head; scale = amax / 448
+# (the largest finite E4M3 value); only Q and K are quantised, and P V stays
+# BF16.  The kernels must decide every E4M3 code exactly as done here, so the
+# rotation and the division by the scale are carried out in float32 in the
+# order stated below; everything after the codes is FP64.
+
+E4M3_MAX = 448.0
+
+
+def round_e4m3(x) -> np.ndarray:
+    """Nearest E4M3 value (1 sign, 4 exponent bits with bias 7, 3 mantissa
+    bits, no infinities; largest finite 448, subnormals k * 2^-9), ties to
+    even, magnitudes beyond the largest finite value saturated to it."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, fe = np.frexp(a)                 # a = f 2^fe with f in [0.5, 1): exponent fe - 1
+    e = np.maximum(fe.astype(np.float64) - 1.0, -6.0)  # below 2^-6 the spacing stays 2^-9
+    step = np.exp2(e - 3.0)             # 3 mantissa bits
+    q = np.round(a / step) * step       # exact: step is a power of two; round() is half-even
+    q = np.minimum(q, E4M3_MAX)
+    return np.copysign(q, x)
+
+
+def fwht_f32(x) -> np.ndarray:
+    """Unnormalised Walsh-Hadamard transform along the last axis (a power of
+    two), in float32, butterfly stages h = 1, 2, 4, ...: at stage h the pair
+    (y[i], y[i + h]) of each block of 2h becomes (y[i] + y[i + h], y[i] - y[i + h]).
+    Each output is formed by the same float32 additions in the same order on
+    every platform, so a quantised code decided from it is reproducible."""
+    y = np.array(x, dtype=np.float32, copy=True)
+    d = y.shape[-1]
+    lead = y.shape[:-1]
+    h = 1
+    while h < d:
+        y = y.reshape(lead + (d // (2 * h), 2, h))
+        a = y[..., 0, :]
+        b = y[..., 1, :]
+        y = np.stack([a + b, a - b], axis=-2).reshape(lead + (d,))
+        h *= 2
+    return y
+
+
+def rotate_f32(x, signs) -> np.ndarray:
+    """x R with R = diag(signs) H / sqrt(d) (H the Sylvester Hadamard matrix,
+    signs +-1), evaluated as the kernels evaluate it: the signs first, then the
+    transform, then one multiplication by the float32 value of 1/sqrt(d).
+    R is orthogonal, so (Q R)(K R)^T = Q K^T."""
+    x = np.asarray(x, dtype=np.float32)
+    s = np.asarray(signs, dtype=np.float32)
+    inv = np.float32(1.0 / np.sqrt(x.shape[-1]))
+    return fwht_f32(x * s) * inv
+
+
+def quantize_e4m3_tiles(x, tile: int = 128):
+    """Per-tile E4M3 quantisation of x [B,H,N,d] (float32): for every head and
+    block of `tile` rows, scale = amax / 448 in float32 (1 for an all-zero
+    tile) and codes = round_e4m3(float32(x / scale)).  Returns the code values
+    (float64, exactly representable) and the scales [B,H,ceil(N/tile)]."""
+    x = np.asarray(x, dtype=np.float32)
+    B, H, N, d = x.shape
+    nt = (N + tile - 1) // tile
+    scales = np.empty((B, H, nt), dtype=np.float32)
+    codes = np.empty(x.shape, dtype=np.float64)
+    for t in range(nt):
+        blk = x[:, :, t * tile:(t + 1) * tile, :]
+        amax = np.abs(blk).max(axis=(2, 3)).astype(np.float32)
+        sc = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+        scales[:, :, t] = sc
+        q = (blk / sc[:, :, None, None]).astype(np.float32)
+        codes[:, :, t * tile:(t + 1) * tile, :] = round_e4m3(q)
+    return codes, scales
+
+
+def attention_fwd_fp8(q, k, v, signs, causal: bool, scale: float, Hkv=None):
+    """The FP8 forward's definition: Q and K rotated by R (incoherent
+    processing) and quantised to E4M3 with per-tile scales; O and LSE are
+    exact attention (FP64) on the dequantised rotated Q, K and on V as given.
+    Returns (O, LSE, (q codes, q scales), (k codes, k scales))."""
+    qr = rotate_f32(q, signs)
+    kr = rotate_f32(k, signs)
+    qc, qs = quantize_e4m3_tiles(qr)
+    kc, ks = quantize_e4m3_tiles(kr)
+    qd = qc * np.repeat(qs.astype(np.float64), 128, axis=2)[:, :, :qc.shape[2], None]
+    kd = kc * np.repeat(ks.astype(np.float64), 128, axis=2)[:, :, :kc.shape[2], None]
+    if Hkv is not None and Hkv != np.asarray(q).shape[1]:
+        o, lse = attention_fwd_gqa(qd, kd, v, causal, scale)
+    else:
+        o, lse = attention_fwd(qd, kd, v, causal, scale)
+    return o, lse, (qc, qs), (kc, ks)

@@ -408,3 +408,143 @@ def test_gqa_rejects_heads_that_do_not_divide(oracle_lib):
     k = np.zeros((1, 2, 4, 2))
     with pytest.raises(ValueError):
         oracle_lib.attention_fwd_gqa(q, k, k, False, 1.0)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) and incoherent processing
+
+def _e4m3_table():
+    """Every finite E4M3 value, decoded from the bit fields of the format
+    (sign, 4-bit exponent with bias 7, 3-bit mantissa; exponent field 0 is
+    subnormal; the all-ones pattern S.1111.111 is NaN)."""
+    vals = []
+    for code in range(256):
+        s, e, m = code >> 7, (code >> 3) & 15, code & 7
+        if e == 15 and m == 7:
+            continue
+        v = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+        vals.append((-v if s else v, code))
+    return vals
+
+
+def test_e4m3_codes_are_fixed_points(oracle_lib):
+    table = _e4m3_table()
+    v = np.array([t[0] for t in table])
+    assert np.array_equal(oracle_lib.round_e4m3(v), v)
+    pos = np.unique(v[v >= 0])
+    assert pos.max() == 448.0 and pos[1] == 2.0 ** -9 and len(pos) == 127
+
+
+def test_e4m3_ties_to_even_and_saturates(oracle_lib):
+    # the midpoint of two neighbours goes to the one whose mantissa is even
+    by_val = {}
+    for v, code in _e4m3_table():
+        if v >= 0:
+            by_val[v] = code
+    pos = sorted(by_val)
+    lo, hi = np.array(pos[:-1]), np.array(pos[1:])
+    mid = (lo + hi) / 2
+    got = oracle_lib.round_e4m3(np.concatenate([mid, -mid]))
+    want = np.where([by_val[a] % 2 == 0 for a in lo], lo, hi)
+    assert np.array_equal(got, np.concatenate([want, -want]))
+    # just off the midpoint the nearer neighbour wins
+    eps = (hi - lo) * 1e-3
+    assert np.array_equal(oracle_lib.round_e4m3(mid - eps), lo)
+    assert np.array_equal(oracle_lib.round_e4m3(mid + eps), hi)
+    # beyond the largest finite value: saturation, not infinity or NaN
+    assert np.array_equal(oracle_lib.round_e4m3([449.0, 1e6, -3e38]), [448.0, 448.0, -448.0])
+    assert oracle_lib.round_e4m3([0.0])[0] == 0.0
+
+
+def test_e4m3_matches_torch_float8(oracle_lib):
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    x = fa_inputs.normal_stream(5, 0, 20000).astype(np.float32) * np.float32(60.0)
+    x = np.clip(x, -448.0, 448.0)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle_lib.round_e4m3(x), ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwht_is_the_sylvester_hadamard_product(oracle_lib, d):
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    x = fa_inputs.normal_stream(7, 0, 6 * d).reshape(6, d)
+    H = scipy_linalg.hadamard(d).astype(np.float64)
+    got = oracle_lib.fwht_f32(x).astype(np.float64)
+    want = x.astype(np.float64) @ H  # H is symmetric
+    assert np.max(np.abs(got - want)) <= 1e-5 * np.max(np.abs(want))
+    # applied twice it is d times the identity
+    twice = oracle_lib.fwht_f32(oracle_lib.fwht_f32(x)).astype(np.float64)
+    assert np.max(np.abs(twice - d * x)) <= 1e-4 * d
+
+
+def test_fwht_butterfly_order_is_fixed(oracle_lib):
+    # exact small case: the first stage pairs neighbours, the last pairs halves
+    x = np.array([1.0, 2.0, 4.0, 8.0], dtype=np.float32)
+    assert np.array_equal(oracle_lib.fwht_f32(x), np.array([15.0, -5.0, -9.0, 3.0], np.float32))
+
+
+def test_rotation_is_orthogonal_and_keeps_scores(oracle_lib):
+    d = 128
+    signs = fa_inputs.random_signs(3, d)
+    assert set(np.unique(signs)) == {-1.0, 1.0}
+    q, k, _, _ = _rand(21, 1, 2, 40, d)
+    qr = oracle_lib.rotate_f32(q, signs).astype(np.float64)
+    kr = oracle_lib.rotate_f32(k, signs).astype(np.float64)
+    s0 = q.astype(np.float64) @ np.swapaxes(k.astype(np.float64), -1, -2)
+    s1 = qr @ np.swapaxes(kr, -1, -2)
+    assert np.max(np.abs(s1 - s0)) <= 1e-4
+    assert np.allclose(np.linalg.norm(qr, axis=-1), np.linalg.norm(q, axis=-1), rtol=1e-5)
+    # the rotation is not the identity, and the signs matter
+    assert np.max(np.abs(qr - q)) > 0.5
+    other = oracle_lib.rotate_f32(q, np.ones(d, np.float32)).astype(np.float64)
+    assert np.max(np.abs(other - qr)) > 0.5
+
+
+def test_tile_quantisation_bounds_and_independence(oracle_lib):
+    x = fa_inputs.normal_stream(9, 0, 2 * 300 * 64).reshape(1, 2, 300, 64)
+    x[0, 1, 128:256] *= np.float32(37.0)      # one tile far larger than the others
+    x[0, 0, 256:] = 0.0                       # an all-zero ragged tail tile
+    codes, scales = oracle_lib.quantize_e4m3_tiles(x)
+    assert scales.shape == (1, 2, 3)
+    assert np.all(np.abs(codes) <= 448.0)
+    assert scales[0, 0, 2] == 1.0 and np.all(codes[0, 0, 256:] == 0.0)
+    for h in range(2):
+        for t in range(3):
+            blk = x[0, h, t * 128:(t + 1) * 128].astype(np.float64)
+            c = codes[0, h, t * 128:(t + 1) * 128]
+            if not np.any(blk):
+                continue
+            amax = np.abs(blk).max()
+            assert np.isclose(scales[0, h, t], amax / 448.0, rtol=1e-6)
+            assert np.abs(c).max() == 448.0           # the tile's largest entry hits the top code
+            err = np.abs(c * scales[0, h, t] - blk)
+            # E4M3 keeps 3 mantissa bits: half a spacing is at most 2^-4 of the
+            # value, and at most 2^-10 * scale among subnormals
+            assert np.all(err <= np.maximum(np.abs(blk) * 2.0 ** -4, 2.0 ** -10 * scales[0, h, t]) * 1.0001)
+    # scaling one tile by a power of two moves only that tile's scale
+    y = x.copy()
+    y[0, 1, :128] *= np.float32(8.0)
+    c2, s2 = oracle_lib.quantize_e4m3_tiles(y)
+    assert np.array_equal(c2, codes)
+    assert s2[0, 1, 0] == 8.0 * scales[0, 1, 0] and np.array_equal(s2[0, :, 1:], scales[0, :, 1:])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_is_close_to_exact_attention(oracle_lib, causal):
+    d = 64
+    q, k, v, _ = _rand(31, 1, 2, 200, d)
+    signs = fa_inputs.random_signs(4, d)
+    o8, lse8, (qc, qs), (kc, ks) = oracle_lib.attention_fwd_fp8(q, k, v, signs, causal, _scale(d))
+    o, lse = oracle_lib.attention_fwd(q, k, v, causal, _scale(d))
+    # E4M3 keeps 3 mantissa bits, so each score moves by a few hundredths
+    # (rows with few keys, early causal rows, show it most); rotating only one
+    # of Q and K, or a wrong scale, moves O by about one (RMS > 0.1)
+    assert np.max(np.abs(o8 - o)) < 0.25 and np.max(np.abs(lse8 - lse)) < 0.1
+    assert np.sqrt(np.mean((o8 - o) ** 2)) < 0.02
+    # and it is FP64 attention on exactly the dequantised rotated Q and K
+    qd = qc * np.repeat(qs.astype(np.float64), 128, axis=2)[:, :, :200, None]
+    kd = kc * np.repeat(ks.astype(np.float64), 128, axis=2)[:, :, :200, None]
+    o2, lse2 = oracle_lib.attention_fwd(qd, kd, v, causal, _scale(d))
+    assert np.array_equal(o2, o8) and np.array_equal(lse2, lse8)
+

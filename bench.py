@@ -41,19 +41,31 @@ WORKLOAD = "training step fwd+bwd, bf16, B=8 H=16 N=2048 d=128, causal, scale=1/
 
 # DRAM traffic of one launch of a kernel at this workload, from the ncu
 # summaries under profiles/; valid only for the kernel source it was measured
-# on (sha256 of its .cu file), else the roofline reports traffic as null.
+# on (sha256 of its .cu file followed by the shared primitives header), else
+# the roofline reports traffic as null.
 CSRC = os.path.join(ROOT, "exact_io_aware_18_gb300", "csrc")
 KERNEL_SRC = {"fwd_bf16": os.path.join(CSRC, "fwd_bf16_sm103.cu"),
               "bwd_dkdv_bf16": os.path.join(CSRC, "bwd_bf16_sm103.cu"),
               "bwd_dq_bf16": os.path.join(CSRC, "bwd_dq_sm103.cu")}
+KERNEL_HDR = os.path.join(CSRC, "sm103_primitives.cuh")
+
+
+def kernel_src_sha256(name: str) -> str:
+    h = hashlib.sha256()
+    for path in (KERNEL_SRC[name], KERNEL_HDR):
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 KERNEL_TRAFFIC = {
     # profiles/kernels_training_step_b8_h16_n2048_d128_causal.md (ncu --set full)
-    "fwd_bf16": {"bytes": 201413376 + 47730688,
-                 "src_sha256": "7af678f8ad2245719cf3ad560c84fd2e3144f9e92dbe4768de62a93e50853ded"},
-    "bwd_dkdv_bf16": {"bytes": 270609664 + 220932608,
-                      "src_sha256": "3f51b0a700edda43dbaef9206612e923e41c46bf70d24c993827bbdbe5b4102d"},
-    "bwd_dq_bf16": {"bytes": 270613760 + 108294912,
-                    "src_sha256": "d70a5e2d980604d6601114c68ee2c0772662181b6f118c9ae9d4d2f4a630c1f0"},
+    "fwd_bf16": {"bytes": 201501440 + 47808000,
+                 "src_sha256": "a87f7316cb4edd5c80c3d57c5089f5275b01349bb1da2240c9045b39b7ef289d"},
+    "bwd_dkdv_bf16": {"bytes": 270640384 + 218950656,
+                      "src_sha256": "bf2c213825688402631586a67f108ad1d2b8d8bbbd0ba2885fd9eb8c3a67a479"},
+    "bwd_dq_bf16": {"bytes": 270698496 + 108191744,
+                    "src_sha256": "168b9eec1cd34cabe7ec22a9c52ca1cd6f4b2ee7d26161b1b958d7cfc46c0230"},
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -392,9 +404,7 @@ def run_gpu(args):
     achieved = kern_flops[dominant] / (kern_ms[dominant] * 1e-3) / 1e12
     traffic = None
     try:
-        src = KERNEL_SRC[dominant]
-        with open(src, "rb") as fsrc:
-            sha = hashlib.sha256(fsrc.read()).hexdigest()
+        sha = kernel_src_sha256(dominant)
         rec = KERNEL_TRAFFIC.get(dominant)
         if rec and rec["bytes"] and rec["src_sha256"] == sha:
             traffic = rec["bytes"]

@@ -213,11 +213,12 @@ def attention_bwd_gqa(q, k, v, do, causal: bool, scale: float, o_storage="exact"
 # channels are spread over all channels.  The pages fix neither the matrix,
 # the tile, the scale rule nor which operands go to FP8; the readings taken
 # here: the matrix is a Hadamard transform with random signs (orthogonal, and
-# applied in O(d log d)); a tile is 128 rows of one head; scale = amax / 448
-# (the largest finite E4M3 value); only Q and K are quantised, and P V stays
-# BF16.  The kernels must decide every E4M3 code exactly as done here, so the
-# rotation and the division by the scale are carried out in float32 in the
-# order stated below; everything after the codes is FP64.
+# applied in O(d log d)); a tile is 128 rows of one head, mapped onto the
+# E4M3 range by the factor 448 / amax (448 the largest finite E4M3 value) and
+# dequantised by amax / 448; only Q and K are quantised, and P V stays BF16.
+# The kernels must decide every E4M3 code exactly as done here, so the
+# rotation and the scaling are carried out in float32 in the order stated
+# below; everything after the codes is FP64.
 
 E4M3_MAX = 448.0
 
@@ -267,21 +268,26 @@ def rotate_f32(x, signs) -> np.ndarray:
 
 
 def quantize_e4m3_tiles(x, tile: int = 128):
-    """Per-tile E4M3 quantisation of x [B,H,N,d] (float32): for every head and
-    block of `tile` rows, scale = amax / 448 in float32 (1 for an all-zero
-    tile) and codes = round_e4m3(float32(x / scale)).  Returns the code values
-    (float64, exactly representable) and the scales [B,H,ceil(N/tile)]."""
+    """Per-tile E4M3 quantisation of x [B,H,N,d] (float32).  For every head and
+    block of `tile` rows with largest magnitude amax > 0: the code of x is
+    round_e4m3(float32(x * m)) with the float32 factor m = 448 / amax, and the
+    tile's dequantisation scale is the float32 value amax / 448 (an all-zero
+    tile has codes 0 and scale 1).  Returns the code values (float64, exactly
+    representable) and the scales [B,H,ceil(N/tile)]."""
     x = np.asarray(x, dtype=np.float32)
     B, H, N, d = x.shape
     nt = (N + tile - 1) // tile
     scales = np.empty((B, H, nt), dtype=np.float32)
     codes = np.empty(x.shape, dtype=np.float64)
+    top = np.float32(E4M3_MAX)
     for t in range(nt):
         blk = x[:, :, t * tile:(t + 1) * tile, :]
         amax = np.abs(blk).max(axis=(2, 3)).astype(np.float32)
-        sc = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-        scales[:, :, t] = sc
-        q = (blk / sc[:, :, None, None]).astype(np.float32)
+        nz = amax > 0
+        safe = np.where(nz, amax, np.float32(1.0)).astype(np.float32)
+        scales[:, :, t] = np.where(nz, safe / top, np.float32(1.0))
+        m = np.where(nz, top / safe, np.float32(0.0)).astype(np.float32)
+        q = (blk * m[:, :, None, None]).astype(np.float32)
         codes[:, :, t * tile:(t + 1) * tile, :] = round_e4m3(q)
     return codes, scales
 

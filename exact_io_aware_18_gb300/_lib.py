@@ -49,6 +49,8 @@ _SIGNATURES = {
     "fa_bwd_gqa": ([_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp], _i),
     "fa_fwd_splitkv_workspace_bytes": ([_i] * 7, _sz),
     "fa_fwd_splitkv": ([_vp] * 5 + [_i] * 6 + [_f, _i, _vp, _sz, _vp], _i),
+    "fa_fp8_quantize": ([_vp] * 4 + [_i] * 3 + [_vp], _i),
+    "fa_fwd_fp8": ([_vp] * 7 + [_i] * 6 + [_f, _vp], _i),
 }
 
 NOALLOC_SCRATCH_BYTES = 8 << 20  # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
@@ -150,6 +152,49 @@ def fa_fwd_gqa(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None
     _expect(lse, "lse", torch.float32, (B, Hq, N))
     _check(load().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
                              int(bool(causal)), float(scale), _stream(stream)), "fa_fwd_gqa")
+
+
+# ----------------------------------------------------------------- FP8 forward
+
+def _host_signs(signs, d: int):
+    """d signs (+1 / -1) as a C float array; the library validates the values."""
+    if isinstance(signs, torch.Tensor):
+        vals = signs.detach().to("cpu", torch.float64).reshape(-1).tolist()
+    else:
+        vals = [float(x) for x in signs]
+    if len(vals) != d:
+        raise ValueError(f"signs must hold d = {d} entries, got {len(vals)}")
+    return (ctypes.c_float * d)(*vals)
+
+
+def fa_fp8_quantize(x, signs, codes, scales, stream=None) -> None:
+    """Rotation by diag(signs) H / sqrt(d) and per-128-row-tile E4M3 codes:
+    x bf16 [B,H,N,d] -> codes uint8 [B,H,N,d], scales float32 [B,H,ceil(N/128)]."""
+    B, H, N, d = _bhnd(x)
+    _expect(x, "x", torch.bfloat16, (B, H, N, d))
+    _expect(codes, "codes", torch.uint8, (B, H, N, d))
+    _expect(scales, "scales", torch.float32, (B, H, (N + 127) // 128))
+    arr = _host_signs(signs, d)
+    _check(load().fa_fp8_quantize(_ptr(x), ctypes.cast(arr, _vp), _ptr(codes), _ptr(scales),
+                                  B * H, N, d, _stream(stream)), "fa_fp8_quantize")
+
+
+def fa_fwd_fp8(q8, q_scale, k8, k_scale, v, o, lse, causal: bool, scale: float,
+               stream=None) -> None:
+    """Forward from E4M3 codes of the rotated Q [B,Hq,N,d] and K [B,Hkv,N,d] and
+    their tile scales; v bf16 [B,Hkv,N,d]; o bf16 [B,Hq,N,d]; lse float32."""
+    B, Hq, Hkv, N, d = _gqa_heads(q8, k8)
+    nt = (N + 127) // 128
+    _expect(q8, "q8", torch.uint8, (B, Hq, N, d))
+    _expect(k8, "k8", torch.uint8, (B, Hkv, N, d))
+    _expect(q_scale, "q_scale", torch.float32, (B, Hq, nt))
+    _expect(k_scale, "k_scale", torch.float32, (B, Hkv, nt))
+    _expect(v, "v", torch.bfloat16, (B, Hkv, N, d))
+    _expect(o, "o", torch.bfloat16, (B, Hq, N, d))
+    _expect(lse, "lse", torch.float32, (B, Hq, N))
+    _check(load().fa_fwd_fp8(_ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale), _ptr(v), _ptr(o),
+                             _ptr(lse), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                             _stream(stream)), "fa_fwd_fp8")
 
 
 def fa_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, workspace=None,

@@ -111,6 +111,24 @@ int make_map_bf16(CUtensorMap* map, const void* ptr, int d, int N, long long BH)
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// [B*H, N, d] E4M3 codes (bytes) viewed as (d, N, B*H) with one 128-row box
+// of d bytes (d = 128: exactly the 128-byte swizzle span).  Rows past N read
+// as zero, the code of +0.
+int make_map_u8(CUtensorMap* map, const void* ptr, int d, int N, long long BH) {
+    EncodeFn enc;
+    if (int rc = get_encode(&enc)) return rc;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d),
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 // FP32 gradient (d, N, B*H) written by TMA stores: 32 x 32 boxes (128-byte
 // rows), 128-byte swizzle.  Rows past N are clipped by the copy engine.
 int make_map_f32_out(CUtensorMap* map, float* ptr, int d, int N, long long BH) {
@@ -374,6 +392,51 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
     }
     if (!workspace && cudaFreeAsync(ws, st) != cudaSuccess && rc == FA_OK) rc = FA_ERR_CUDA;
     return rc;
+}
+
+int fa_fp8_quantize(const void* x, const float* signs, void* codes, float* scales, int BH, int N,
+                    int d, void* stream) {
+    if (!signs) return FA_ERR_INVALID_ARG;
+    if (int rc = check_ptrs({x, codes, scales})) return rc;
+    if (int rc = check_shape(1, BH, N, d, 1.f)) return rc;
+    fa::Fp8QuantArgs a{};
+    for (int i = 0; i < d; ++i) {
+        if (signs[i] != 1.f && signs[i] != -1.f) return FA_ERR_INVALID_ARG;
+        a.signs.s[i] = signs[i];
+    }
+    a.x = x;
+    a.codes = codes;
+    a.scales = scales;
+    a.BH = BH;
+    a.N = N;
+    a.d = d;
+    a.inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    return launch_rc(fa::launch_fp8_rotate_quantize(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+               const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
+               int causal, float scale, void* stream) {
+    if (int rc = check_ptrs({q8, q_scale, k8, k_scale, v, o, lse})) return rc;
+    if (int rc = check_shape(B, Hq, N, d, scale)) return rc;
+    if (int rc = check_heads(Hq, Hkv)) return rc;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    unsigned int* status;
+    if (int rc = status_ptr(&status)) return rc;
+    const long long BH = static_cast<long long>(B) * Hq;
+    const long long BHkv = static_cast<long long>(B) * Hkv;
+    CUtensorMap tq, tk, tv, to;
+    if (int rc = make_map_u8(&tq, q8, d, N, BH)) return rc;
+    if (int rc = make_map_u8(&tk, k8, d, N, BHkv)) return rc;
+    if (int rc = make_map_bf16(&tv, v, d, N, BHkv)) return rc;
+    if (int rc = make_map_bf16(&to, o, d, N, BH)) return rc;
+    unsigned int* work;
+    int sms;
+    if (int rc = work_slot(&work, &sms)) return rc;
+    fa::FwdArgs a{&tq, &tk, &tv, &to, lse, B, Hq, N, d, Hkv, causal ? 1 : 0,
+                  scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms,
+                  /*Nk=*/N, /*n_splits=*/1, /*chunk_tiles=*/0, nullptr, nullptr, q_scale, k_scale};
+    return launch_rc(fa::launch_fwd_fp8(a, static_cast<cudaStream_t>(stream)));
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {

@@ -35,10 +35,33 @@ struct FwdArgs {
     int chunk_tiles;
     float* o_part;
     float* lse_part;
+    // FP8 forward: tm_q and tm_k view E4M3 codes (d, N, B*H) with one 128 x d
+    // box; q_scale [B*H][ceil(N/128)] and k_scale [B*Hkv][ceil(N/128)] are the
+    // tiles' dequantisation scales.  Null for the BF16 forward.
+    const float* q_scale;
+    const float* k_scale;
 };
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_splitkv_bf16(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream);
+
+// Rotation by diag(s) H / sqrt(d) and per-128-row-tile E4M3 quantisation of
+// one BF16 tensor [BH][N][d]: codes [BH][N][d] (bytes), scales [BH][ceil(N/128)].
+struct Fp8Signs {
+    float s[128];  // +1 / -1, the first d entries used
+};
+
+struct Fp8QuantArgs {
+    const void* x;
+    void* codes;
+    float* scales;
+    int BH, N, d;
+    float inv_sqrt_d;  // float32 value of 1 / sqrt(d)
+    Fp8Signs signs;
+};
+
+cudaError_t launch_fp8_rotate_quantize(const Fp8QuantArgs& a, cudaStream_t stream);
 
 // Merge of the split-KV partials: per query row, O = sum_s w_s O_s / sum_s w_s
 // and LSE = m + ln sum_s w_s with w_s = exp(LSE_s - m), m = max_s LSE_s;

@@ -51,6 +51,7 @@
 // bounded (see sm103_primitives.cuh); a CTA that gives up tells the others
 // through its abort flag and every role leaves at its next wait.
 #include "fa_internal.h"
+#include "sm103_fp8.cuh"
 #include "sm103_primitives.cuh"
 
 namespace fa {
@@ -62,18 +63,21 @@ constexpr uint32_t kRegsSoftmax = 216;  // warps 4-11 after the split
 static_assert(128 * (kRegsLight + 2 * kRegsSoftmax) <= 384 * 168, "register split");
 constexpr int kStoreThread = 128;       // softmax thread that issues the O stores
 
-template <int D>
+template <int D, bool FP8 = false>
 struct FwdCfg {
     static constexpr int BM = 128;                    // query rows per tile
     static constexpr int BN = 128;                    // keys per K/V tile
     static constexpr int KB = D / 64;                 // 64-column (128-byte) boxes per row
     static constexpr int BOX_BYTES = 128 * 64 * 2;    // one 128 x 64 bf16 box
     static constexpr int TILE_BYTES = KB * BOX_BYTES; // one 128 x D bf16 tile
+    // FP8: Q and K tiles are 128 x D E4M3 codes, one 128-byte-wide box (D = 128).
+    static constexpr int QK_BYTES = FP8 ? 128 * D : TILE_BYTES;
     static constexpr int NS = (D == 128) ? 2 : 4;     // K/V ring depth
     static constexpr int QUEUE = 4;                   // claimed-tile queue depth
-    static constexpr int OFF_Q = 0;                   // two Q buffers
+    // Two Q buffers of a BF16 tile each: the O tile is staged over them.
+    static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
-    static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + NS * QK_BYTES;
     static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int OFF_XCH = OFF_BAR + BAR_BYTES;  // row maxima and sums of the halves
@@ -115,7 +119,7 @@ struct FwdBars {
     static constexpr int COUNT = DONE + 1;
 };
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool FP8>
 __global__ void __launch_bounds__(384, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -124,8 +128,10 @@ __global__ void __launch_bounds__(384, 1)
                     int BH, int Hq, int n_rep, int n_tiles, int group, float scale_log2,
                     unsigned int* status, unsigned long long timeout_ns, unsigned int* work,
                     int Nk, int n_splits, int chunk_tiles, float* __restrict__ o_part,
-                    float* __restrict__ lse_part) {
-    using C = FwdCfg<D>;
+                    float* __restrict__ lse_part, const float* __restrict__ q_scale,
+                    const float* __restrict__ k_scale) {
+    using C = FwdCfg<D, FP8>;
+    static_assert(!(FP8 && (SPLIT || D != 128)), "the FP8 forward is built for d = 128, no split");
     using Bar = FwdBars<C::NS, C::QUEUE>;
     static_assert(8 * Bar::COUNT + 8 <= C::BAR_BYTES, "barrier area");
     extern __shared__ uint8_t smem_raw[];
@@ -260,10 +266,15 @@ __global__ void __launch_bounds__(384, 1)
                     mbar_arrive(bar(Bar::ITEM_FULL + slot));
                     if (item < 0) break;
                     const Work w = work_of(item);
-                    mbar_arrive_expect_tx(bar(Bar::Q_FULL + qb), C::TILE_BYTES);
-                    for (int kb = 0; kb < C::KB; ++kb)
-                        tma_load_3d(s_q + qb * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_q,
-                                    bar(Bar::Q_FULL + qb), kb * 64, w.qt * C::BM, w.bh);
+                    mbar_arrive_expect_tx(bar(Bar::Q_FULL + qb), C::QK_BYTES);
+                    if constexpr (FP8) {
+                        tma_load_3d(s_q + qb * C::TILE_BYTES, &tm_q, bar(Bar::Q_FULL + qb), 0,
+                                    w.qt * C::BM, w.bh);
+                    } else {
+                        for (int kb = 0; kb < C::KB; ++kb)
+                            tma_load_3d(s_q + qb * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_q,
+                                        bar(Bar::Q_FULL + qb), kb * 64, w.qt * C::BM, w.bh);
+                    }
                     q_issued = k + 1;
                 }
                 // After giving up, still draw numbers until one fails, so that
@@ -296,10 +307,15 @@ __global__ void __launch_bounds__(384, 1)
                         const int use = g / C::NS;
                         if (use > 0) ok = mbar_wait(bar(Bar::K_EMPTY + st), (use - 1) & 1, wc);
                         if (!ok) break;
-                        mbar_arrive_expect_tx(bar(Bar::K_FULL + st), C::TILE_BYTES);
-                        for (int kb = 0; kb < C::KB; ++kb)
-                            tma_load_3d(s_k + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_k,
-                                        bar(Bar::K_FULL + st), kb * 64, j * C::BN, bkv);
+                        mbar_arrive_expect_tx(bar(Bar::K_FULL + st), C::QK_BYTES);
+                        if constexpr (FP8) {
+                            tma_load_3d(s_k + st * C::QK_BYTES, &tm_k, bar(Bar::K_FULL + st), 0,
+                                        j * C::BN, bkv);
+                        } else {
+                            for (int kb = 0; kb < C::KB; ++kb)
+                                tma_load_3d(s_k + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_k,
+                                            bar(Bar::K_FULL + st), kb * 64, j * C::BN, bkv);
+                        }
                         k_issued = g + 1;
                         if (use > 0) ok = mbar_wait(bar(Bar::V_EMPTY + st), (use - 1) & 1, wc);
                         if (!ok) break;
@@ -352,7 +368,9 @@ __global__ void __launch_bounds__(384, 1)
                         // Issuer A: S_j = Q K_j^T into buffer g & 1 once the softmax
                         // warps have read S_{g-2} out of it (the next phase of that
                         // S_EMPTY needs S_g itself, so the wait cannot miss it).
-                        ok = mbar_wait(bar(Bar::QT_FULL), k & 1, wc);
+                        // Q in TMEM (BF16) or Q's E4M3 tile in shared memory (FP8).
+                        if constexpr (FP8) ok = mbar_wait(bar(Bar::Q_FULL + (k & 1)), (k >> 1) & 1, wc);
+                        else ok = mbar_wait(bar(Bar::QT_FULL), k & 1, wc);
                         for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
                             const int st = g % C::NS;
                             const int b = g & 1;
@@ -360,19 +378,31 @@ __global__ void __launch_bounds__(384, 1)
                             ok = ok && mbar_wait(bar(Bar::K_FULL + st), (g / C::NS) & 1, wc);
                             if (!ok) break;
                             tc_fence_after();
-                            const uint32_t k_tile = s_k + st * C::TILE_BYTES;
+                            const uint32_t k_tile = s_k + st * C::QK_BYTES;
                             const uint32_t d_tmem = tmem + (b ? C::COL_S1 : C::COL_S0);
+                            if constexpr (FP8) {
+                                // E4M3 codes, 32 bytes of K per instruction, both
+                                // operands K-major in shared memory.
+                                constexpr uint32_t id_s8 = idesc_e4m3(128, 128);
+                                const uint32_t q_tile = s_q + (k & 1) * C::TILE_BYTES;
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                                mma_ts(d_tmem, tmem + C::COL_Q + kk * 8,
-                                       smem_desc_sw128(k_tile + koff, 16, 1024), id_s, kk > 0);
+                                for (int kk = 0; kk < D / 32; ++kk)
+                                    mma_ss_f8(d_tmem, smem_desc_sw128(q_tile + kk * 32, 16, 1024),
+                                              smem_desc_sw128(k_tile + kk * 32, 16, 1024), id_s8,
+                                              kk > 0);
+                            } else {
+#pragma unroll
+                                for (int kk = 0; kk < D / 16; ++kk) {
+                                    const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                                    mma_ts(d_tmem, tmem + C::COL_Q + kk * 8,
+                                           smem_desc_sw128(k_tile + koff, 16, 1024), id_s, kk > 0);
+                                }
                             }
                             tc_commit(bar(Bar::S_FULL + b));
                             tc_commit(bar(Bar::K_EMPTY + st));
                         }
                         // Q's TMEM columns are free once these MMAs have finished.
-                        if (ok) tc_commit(bar(Bar::QT_EMPTY));
+                        if (!FP8 && ok) tc_commit(bar(Bar::QT_EMPTY));
                     }
                 }
             }
@@ -412,10 +442,11 @@ __global__ void __launch_bounds__(384, 1)
             // Q into TMEM as BF16 pairs (the A operand of S = Q K^T): this
             // thread's row, elements [h d/2, (h+1) d/2), read from the swizzled
             // tile, once the previous tile's S MMAs have finished with it.
-            bool ok = __all_sync(0xffffffffu,
-                                 mbar_wait(bar(Bar::Q_FULL + qb), (k >> 1) & 1, wc) &&
-                                     (k == 0 || mbar_wait(bar(Bar::QT_EMPTY), (k - 1) & 1, wc)));
-            if (ok) {
+            // (FP8: the S MMAs read Q's codes from shared memory; nothing to copy.)
+            bool ok = FP8 || __all_sync(0xffffffffu,
+                                        mbar_wait(bar(Bar::Q_FULL + qb), (k >> 1) & 1, wc) &&
+                                            (k == 0 || mbar_wait(bar(Bar::QT_EMPTY), (k - 1) & 1, wc)));
+            if (!FP8 && ok) {
                 tc_fence_after();
                 uint32_t qw[D / 4];
 #pragma unroll
@@ -439,8 +470,19 @@ __global__ void __launch_bounds__(384, 1)
 
             float m_run = -INFINITY;  // running max, base-2 units of scale * S
             float l_run = 0.f;        // this half's running sum of 2^(x - m_run)
+            // FP8: S holds code products; Q's tile scale (and below K's) turn
+            // them into scores.
+            const float c_q = FP8 ? scale_log2 * q_scale[static_cast<long long>(bh) * n_tiles + qt]
+                                  : scale_log2;
+            const int bkv = (bh / Hq) * (Hq / n_rep) + (bh % Hq) / n_rep;
             for (int j = w.j0; j < w.j1; ++j, ++g) {
                 const int b = g & 1;
+                // Factor from S to base-2 exponents for this key tile (at
+                // least FLT_MIN, so that masked entries stay -inf).
+                const float c_s =
+                    FP8 ? fmaxf(c_q * k_scale[static_cast<long long>(bkv) * n_kv_tiles + j],
+                                1.17549435e-38f)
+                        : scale_log2;
                 const uint32_t t_s = t_lane + (b ? C::COL_S1 : C::COL_S0) + 64 * h;
                 // A failed wait is carried to the pair barrier rather than
                 // breaking here, so that both warps leave the loop together.
@@ -475,7 +517,7 @@ __global__ void __launch_bounds__(384, 1)
                 xch[(b * 2 + h) * 128 + row] = mx;
                 ok = named_bar_and(pair_bar, 64, okw);
                 if (!ok) break;
-                const float m_tile = fmaxf(mx, xch[(b * 2 + (h ^ 1)) * 128 + row]) * scale_log2;
+                const float m_tile = fmaxf(mx, xch[(b * 2 + (h ^ 1)) * 128 + row]) * c_s;
                 const bool rescale = m_tile > m_run + 8.0f;
                 float alpha = 1.f;
                 if (rescale) {
@@ -487,8 +529,8 @@ __global__ void __launch_bounds__(384, 1)
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2_approx(fmaf(s[2 * e], scale_log2, neg_m));
-                    const float p1 = ex2_approx(fmaf(s[2 * e + 1], scale_log2, neg_m));
+                    const float p0 = ex2_approx(fmaf(s[2 * e], c_s, neg_m));
+                    const float p1 = ex2_approx(fmaf(s[2 * e + 1], c_s, neg_m));
                     sum += p0 + p1;
                     pk[e] = pack_bf16x2(p0, p1);
                 }
@@ -616,10 +658,10 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool FP8 = false>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
-    using C = FwdCfg<D>;
-    auto kern = fwd_bf16_kernel<D, CAUSAL, SPLIT>;
+    using C = FwdCfg<D, FP8>;
+    auto kern = fwd_bf16_kernel<D, CAUSAL, SPLIT, FP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -632,7 +674,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
         *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse, a.N, a.B * a.H, a.H, a.H / a.Hkv, n_tiles,
         group, a.scale_log2, a.status, a.timeout_ns, a.work, a.Nk, a.n_splits, a.chunk_tiles,
-        a.o_part, a.lse_part);
+        a.o_part, a.lse_part, a.q_scale, a.k_scale);
     return cudaGetLastError();
 }
 
@@ -648,6 +690,12 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_fwd_splitkv_bf16(const FwdArgs& a, cudaStream_t stream) {
     return a.d == 64 ? launch_fwd_t<64, false, true>(a, stream)
                      : launch_fwd_t<128, false, true>(a, stream);
+}
+
+cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
+    if (a.d != 128) return cudaErrorInvalidValue;
+    return a.causal ? launch_fwd_t<128, true, false, true>(a, stream)
+                    : launch_fwd_t<128, false, false, true>(a, stream);
 }
 
 }  // namespace fa

@@ -165,6 +165,41 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int n_splits,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* FP8 forward ("FlashAttention scaling, multi-GPU training and weight
+ * quantization", section 1, FlashAttention-3, FP8 low-precision support):
+ * block quantisation, each small tile with its own scale, and incoherent
+ * processing, Q and K multiplied by a random orthogonal matrix before they are
+ * quantised.  Two calls: fa_fp8_quantize once for Q and once for K, then
+ * fa_fwd_fp8.
+ *
+ * fa_fp8_quantize: y = x R with R = diag(signs) H / sqrt(d) (H the Sylvester
+ * Hadamard matrix, so R is orthogonal and Q R (K R)^T = Q K^T), then per
+ * 128-row tile of each head, with amax = max |y| over the tile:
+ *     codes = E4M3(y * (448 / amax)), round to nearest even, saturating;
+ *     scale = amax / 448  (an all-zero tile: codes 0, scale 1).
+ * All float32 steps are rounded in that order (the butterflies of the
+ * transform in stages h = 1, 2, 4, ...: (y_i, y_i+h) -> (y_i + y_i+h,
+ * y_i - y_i+h)), so the codes are reproducible bit for bit.
+ *   x      : device, bf16 [BH, N, d], 16-byte aligned; d = 64 or 128.
+ *   signs  : HOST array of d floats, each +1 or -1 (FA_ERR_INVALID_ARG
+ *            otherwise); read during the call only.
+ *   codes  : device, E4M3 bytes [BH, N, d], 16-byte aligned.
+ *   scales : device, float [BH, ceil(N / 128)], 16-byte aligned.
+ *
+ * fa_fwd_fp8: attention with S = (Q R)(K R)^T computed from the codes on the
+ * FP8 tensor cores (FP32 accumulation) and multiplied by the Q and K tile
+ * scales; P V in BF16 as in fa_fwd.  Output O (bf16 [B,Hq,N,d]) and LSE
+ * (float [B,Hq,N]) as fa_fwd_gqa.  d must be 128 (FA_ERR_UNSUPPORTED).
+ *   q8, q_scale : fa_fp8_quantize of q [B,Hq,N,d] (BH = B*Hq).
+ *   k8, k_scale : fa_fp8_quantize of k [B,Hkv,N,d] with the same signs.
+ *   v           : bf16 [B,Hkv,N,d], not rotated.
+ * All device pointers 16-byte aligned. */
+int fa_fp8_quantize(const void* x, const float* signs, void* codes, float* scales,
+                    int BH, int N, int d, void* stream);
+int fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+               const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
+               int causal, float scale, void* stream);
+
 /* Size of the scratch array built into the library for fa_bwd_noalloc:
  * 8 MiB, i.e. B * H * roundup(N, 128) <= 1048576. */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)

@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("fa_fwd", "fa_bwd", "fa_fwd_f32", "fa_bwd_f32", "fa_bwd_workspace_bytes",
                  "fa_error_string", "fa_device_status", "fa_bwd_preprocess", "fa_bwd_dkdv",
-                 "fa_bwd_dq", "fa_fwd_gqa", "fa_bwd_gqa"):
+                 "fa_bwd_dq", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fp8_quantize", "fa_fwd_fp8"):
         assert must in names
 
 
@@ -147,3 +147,36 @@ def test_splitkv_workspace_follows_the_split_plan(fa):
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 4, 3, 4096, 128, 1) == per
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 2, 3, 4096, 96, 1) == 0
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 4, 3, 3, 4096, 128, 1) == 0   # 3 does not divide 4
+
+
+def test_fp8_argument_checks_before_launch(fa):
+    lib = fa.load()
+    P = 0x10000
+    signs = (ctypes.c_float * 128)(*([1.0, -1.0] * 64))
+    bad = (ctypes.c_float * 128)(*([1.0] * 127 + [0.5]))
+    sp = ctypes.cast(signs, ctypes.c_void_p)
+    def quant(s=sp, x=P, BH=4, N=300, d=128):
+        return lib.fa_fp8_quantize(x, s, P, P, BH, N, d, None)
+    assert quant(s=None) == fa.FA_ERR_INVALID_ARG
+    assert quant(s=ctypes.cast(bad, ctypes.c_void_p)) == fa.FA_ERR_INVALID_ARG   # not +-1
+    assert quant(x=0) == fa.FA_ERR_INVALID_ARG
+    assert quant(x=P + 8) == fa.FA_ERR_MISALIGNED
+    assert quant(N=0) == fa.FA_ERR_INVALID_ARG
+    assert quant(d=96) == fa.FA_ERR_UNSUPPORTED
+
+    def fwd(B=1, Hq=4, Hkv=2, N=256, d=128, scale=0.125, ptrs=None):
+        ptrs = ptrs or [P] * 7
+        return lib.fa_fwd_fp8(*ptrs, B, Hq, Hkv, N, d, 1, scale, None)
+    assert fwd(d=64) == fa.FA_ERR_UNSUPPORTED            # the FP8 forward is built for d = 128
+    assert fwd(Hkv=3) == fa.FA_ERR_INVALID_ARG           # 3 does not divide 4
+    assert fwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert fwd(ptrs=[P, 0, P, P, P, P, P]) == fa.FA_ERR_INVALID_ARG   # no Q scales
+    assert fwd(ptrs=[P, P, P, P + 4, P, P, P]) == fa.FA_ERR_MISALIGNED
+
+
+def test_fp8_binding_checks_signs(fa):
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):
+        fa._lib._host_signs([1.0, -1.0], 128)
+    arr = fa._lib._host_signs(torch.tensor([1.0, -1.0] * 32), 64)
+    assert list(arr)[:4] == [1.0, -1.0, 1.0, -1.0]

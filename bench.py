@@ -178,11 +178,16 @@ def oracle_cores():
 # ---------------------------------------------------------------- GPU arm
 
 def _timed(torch, stream, fn, iters):
+    """Mean device time of fn over iters back-to-back launches.  A GPU-side
+    sleep queued first keeps the device busy while the host queues every
+    launch, so that calls shorter than their host-side cost (argument checks,
+    tensor-map encoding) are still timed on the device alone."""
     for _ in range(3):
         fn()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(4_000_000)  # about 2 ms of GPU clock cycles
     e0.record(stream)
     for _ in range(iters):
         fn()
@@ -195,7 +200,10 @@ def measure_next_rows(fa, torch, q, k, v, do, stream, iters=20):
     """Rows beyond the training step, timed after (outside) its timed region on
     the same seeded inputs.  Grouped-query attention: the training-step shape
     with 4 query heads per K/V head (K, V: their first H/4 heads)."""
+    import fa_inputs
     scale = fa.default_scale(D)
+    peaks, _ = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     hkv = H // 4
     kg = k[:, :hkv].contiguous()
     vg = v[:, :hkv].contiguous()
@@ -231,11 +239,37 @@ def measure_next_rows(fa, torch, q, k, v, do, stream, iters=20):
                                                               dws, stream), iters)
     dec_bytes = (2 * db * dhkv * dnk * D * 2 + 2 * db * dhq * dnq * D * 2 + db * dhq * dnq * 4)
     dec_flops = 4.0 * db * dhq * dnq * dnk * D
-    peaks, _ = load_peaks()
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # FP8 forward with incoherent processing at the training-step shape: Q and
+    # K rotated and quantised (HBM-bound), then the forward from their codes.
+    signs = fa._lib._host_signs(fa_inputs.random_signs(SEED, D), D)
+    q8 = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
+    k8 = torch.empty(k.shape, dtype=torch.uint8, device=q.device)
+    qs = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device=q.device)
+    ks = torch.empty_like(qs)
+    quant_ms = _timed(torch, stream, lambda: fa.fa_fp8_quantize(q, signs, q8, qs, stream), iters)
+    fa.fa_fp8_quantize(k, signs, k8, ks, stream)
+    fp8_ms = _timed(torch, stream, lambda: fa.fa_fwd_fp8(q8, qs, k8, ks, v, o, lse, CAUSAL, scale,
+                                                          stream), iters)
+    bf16_ms = _timed(torch, stream, lambda: fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream),
+                     iters)
+    # per tensor: BF16 read, E4M3 codes and one FP32 scale per 128-row tile written
+    quant_bytes = B * H * N * D * 3 + B * H * ((N + 127) // 128) * 4
     if fa.fa_device_status(clear=True) != fa.FA_OK:
         raise RuntimeError("a kernel reported a timed-out wait in the next-row measurements")
     return {
+        "fp8_forward": {
+            "workload": f"B={B} H={H} N={N} d={D} causal: Q, K rotated by a random-sign Hadamard "
+                        "transform and quantised to E4M3 per 128-row tile; S from the codes on "
+                        "kind::f8f6f4; P V in BF16",
+            "quantize_ms_per_tensor": round(quant_ms, 4),
+            "quantize_bound": "hbm",
+            "quantize_algorithmic_bytes": quant_bytes,
+            "quantize_gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
+            "quantize_frac_of_hbm": round(quant_bytes / (quant_ms * 1e-3) / 1e9 / hbm, 4),
+            "fwd_ms": round(fp8_ms, 4),
+            "fwd_tflops": round(f_fwd / (fp8_ms * 1e-3) / 1e12, 2),
+            "bf16_fwd_ms_same_inputs": round(bf16_ms, 4),
+            "total_ms_quantize_q_k_and_fwd": round(2 * quant_ms + fp8_ms, 4)},
         "splitkv_decode": {
             "workload": f"B={db} Hq={dhq} Hkv={dhkv} Nq={dnq} Nk={dnk} d={D}, bf16, no mask, "
                         "library-chosen splits",

@@ -15,6 +15,7 @@ import math
 
 import torch
 
+from . import _lib
 from ._lib import (FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT, FA_ERR_INVALID_ARG, FA_ERR_MISALIGNED,
                    FA_ERR_NO_MEMORY, FA_ERR_UNSUPPORTED, FA_OK, FaError, error_string, fa_bwd,
                    fa_bwd_dkdv, fa_bwd_dq, fa_bwd_f32, fa_bwd_gqa, fa_bwd_noalloc,
@@ -89,6 +90,7 @@ def attention_fwd_fp8(q, k, v, signs, causal: bool = False, scale: float | None 
     O (bf16) and LSE (float32)."""
     B, H, N, d = q.shape
     scale = default_scale(d) if scale is None else scale
+    signs = _lib._host_signs(signs, d)
     q8, qs = fp8_quantize(q, signs, stream)
     k8, ks = fp8_quantize(k, signs, stream)
     o = torch.empty_like(q)

@@ -157,7 +157,10 @@ def fa_fwd_gqa(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None
 # ----------------------------------------------------------------- FP8 forward
 
 def _host_signs(signs, d: int):
-    """d signs (+1 / -1) as a C float array; the library validates the values."""
+    """d signs (+1 / -1) as a C float array (returned as is if it already is
+    one of length d); the library validates the values."""
+    if isinstance(signs, ctypes.Array) and len(signs) == d:
+        return signs
     if isinstance(signs, torch.Tensor):
         vals = signs.detach().to("cpu", torch.float64).reshape(-1).tolist()
     else:

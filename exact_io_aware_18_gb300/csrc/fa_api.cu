@@ -112,8 +112,8 @@ int make_map_bf16(CUtensorMap* map, const void* ptr, int d, int N, long long BH)
 }
 
 // [B*H, N, d] E4M3 codes (bytes) viewed as (d, N, B*H) with one 128-row box
-// of d bytes (d = 128: exactly the 128-byte swizzle span).  Rows past N read
-// as zero, the code of +0.
+// of d bytes: 128-byte swizzle at d = 128 (exactly its span), none at d = 64.
+// Rows past N read as zero, the code of +0; stores past N are dropped.
 int make_map_u8(CUtensorMap* map, const void* ptr, int d, int N, long long BH) {
     EncodeFn enc;
     if (int rc = get_encode(&enc)) return rc;
@@ -124,7 +124,8 @@ int make_map_u8(CUtensorMap* map, const void* ptr, int d, int N, long long BH) {
     cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
@@ -404,13 +405,24 @@ int fa_fp8_quantize(const void* x, const float* signs, void* codes, float* scale
         if (signs[i] != 1.f && signs[i] != -1.f) return FA_ERR_INVALID_ARG;
         a.signs.s[i] = signs[i];
     }
-    a.x = x;
-    a.codes = codes;
+    unsigned int* status;
+    unsigned int* unused;
+    int sms;
+    if (int rc = status_ptr(&status)) return rc;
+    if (int rc = work_slot(&unused, &sms)) return rc;
+    CUtensorMap tx, tc;
+    if (int rc = make_map_bf16(&tx, x, d, N, BH)) return rc;
+    if (int rc = make_map_u8(&tc, codes, d, N, BH)) return rc;
+    a.tm_x = &tx;
+    a.tm_codes = &tc;
     a.scales = scales;
     a.BH = BH;
     a.N = N;
     a.d = d;
     a.inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    a.status = status;
+    a.timeout_ns = g_timeout_ns.load();
+    a.num_sms = sms;
     return launch_rc(fa::launch_fp8_rotate_quantize(a, static_cast<cudaStream_t>(stream)));
 }
 

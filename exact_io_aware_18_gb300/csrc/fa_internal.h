@@ -48,17 +48,23 @@ cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream);
 
 // Rotation by diag(s) H / sqrt(d) and per-128-row-tile E4M3 quantisation of
 // one BF16 tensor [BH][N][d]: codes [BH][N][d] (bytes), scales [BH][ceil(N/128)].
+// tm_x views x like the forward's BF16 maps; tm_codes views the codes as
+// (d, N, BH) bytes with one 128-row box (128-byte swizzle at d = 128, none at
+// d = 64).
 struct Fp8Signs {
     float s[128];  // +1 / -1, the first d entries used
 };
 
 struct Fp8QuantArgs {
-    const void* x;
-    void* codes;
+    const CUtensorMap* tm_x;
+    const CUtensorMap* tm_codes;
     float* scales;
     int BH, N, d;
     float inv_sqrt_d;  // float32 value of 1 / sqrt(d)
     Fp8Signs signs;
+    unsigned int* status;
+    unsigned long long timeout_ns;
+    int num_sms;
 };
 
 cudaError_t launch_fp8_rotate_quantize(const Fp8QuantArgs& a, cudaStream_t stream);

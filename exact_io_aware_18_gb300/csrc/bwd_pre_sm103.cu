@@ -10,8 +10,10 @@
 // Efficiency", section "The Flash Attention algorithm", recomputation).
 //
 // Each thread reads 16-byte vectors, 8 bf16 of O and of dO; d/8 threads share
-// a row and reduce with warp shuffles.  The grid is
-// a multiple of the SM count with a grid-stride loop over rows.
+// a row and reduce with warp shuffles.  A warp owns 32 / (d/8) consecutive
+// rows per group and issues the loads of two groups before it reduces any,
+// so that enough bytes are in flight to keep HBM busy; warps stride over the
+// rows with the whole grid (at most full occupancy on every SM).
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -21,6 +23,7 @@ namespace fa {
 namespace {
 
 constexpr int kPreThreads = 256;
+constexpr int kPreGroups = 2;
 
 template <int D>
 __global__ void __launch_bounds__(kPreThreads)
@@ -28,21 +31,39 @@ __global__ void __launch_bounds__(kPreThreads)
                         const float* __restrict__ lse, float* __restrict__ delta,
                         float* __restrict__ lse2, int N, int n_pad,
                         long long total_rows) {
-    constexpr int TPR = D / 8;                  // threads per row
-    constexpr int RPB = kPreThreads / TPR;      // rows per block per pass
-    const int sub = threadIdx.x % TPR;
-    for (long long r = static_cast<long long>(blockIdx.x) * RPB + threadIdx.x / TPR;
-         r < total_rows; r += static_cast<long long>(gridDim.x) * RPB) {
-        const long long bh = r / n_pad;
-        const int i = static_cast<int>(r - bh * n_pad);
-        float part = 0.f;
-        const bool real = i < N;
-        if (real) {
-            const long long row = bh * N + i;
-            const uint4 a = o[row * (D / 8) + sub];
-            const uint4 b = dO[row * (D / 8) + sub];
-            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+    constexpr int TPR = D / 8;          // threads per row
+    constexpr int RW = 32 / TPR;        // rows per warp and group
+    constexpr int U = kPreGroups;       // groups whose loads are in flight together
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % TPR;
+    const long long warp_id = (static_cast<long long>(blockIdx.x) * kPreThreads + threadIdx.x) / 32;
+    const long long n_warps = static_cast<long long>(gridDim.x) * (kPreThreads / 32);
+    // total_rows is a multiple of 128 and RW * U divides 128, so every row of
+    // a warp's batch exists and the shuffles below see the whole warp.
+    for (long long r0 = warp_id * (RW * U); r0 < total_rows; r0 += n_warps * (RW * U)) {
+        uint4 a[U], b[U];
+        bool real[U];
+        long long row[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long r = r0 + u * RW + lane / TPR;
+            const long long bh = r / n_pad;
+            const int i = static_cast<int>(r - bh * n_pad);
+            real[u] = i < N;
+            row[u] = bh * N + i;
+            if (real[u]) {
+                a[u] = o[row[u] * (D / 8) + sub];
+                b[u] = dO[row[u] * (D / 8) + sub];
+            } else {
+                a[u] = make_uint4(0u, 0u, 0u, 0u);
+                b[u] = a[u];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[u]);
+            float part = 0.f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 x = __bfloat1622float2(a2[e]);
@@ -50,13 +71,14 @@ __global__ void __launch_bounds__(kPreThreads)
                 part = fmaf(x.x, y.x, part);
                 part = fmaf(x.y, y.y, part);
             }
-        }
 #pragma unroll
-        for (int off = TPR / 2; off > 0; off >>= 1)
-            part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (sub == 0) {
-            delta[r] = real ? part : 0.f;
-            lse2[r] = real ? lse[bh * N + i] * 1.4426950408889634f : INFINITY;
+            for (int off = TPR / 2; off > 0; off >>= 1)
+                part += __shfl_xor_sync(0xffffffffu, part, off);
+            if (sub == 0) {
+                const long long r = r0 + u * RW + lane / TPR;
+                delta[r] = real[u] ? part : 0.f;
+                lse2[r] = real[u] ? lse[row[u]] * 1.4426950408889634f : INFINITY;
+            }
         }
     }
 }
@@ -82,18 +104,19 @@ cudaError_t launch_bwd_pre_bf16(const BwdPreArgs& a, cudaStream_t stream) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long total = static_cast<long long>(a.BH) * a.n_pad;
-    const int rpb = kPreThreads / (a.d / 8);
-    long long blocks = (total + rpb - 1) / rpb;
-    const long long cap = static_cast<long long>(sms) * 16;
+    const int rows_per_block = (kPreThreads / 32) * (32 / (a.d / 8)) * kPreGroups;
+    long long blocks = (total + rows_per_block - 1) / rows_per_block;
+    auto kern = a.d == 64 ? bwd_pre_bf16_kernel<64> : bwd_pre_bf16_kernel<128>;
+    // One wave: as many blocks as are resident at once, striding over the rows.
+    int per_sm = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPreThreads, 0) !=
+            cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const long long cap = static_cast<long long>(sms) * per_sm;
     if (blocks > cap) blocks = cap;
-    if (a.d == 64)
-        bwd_pre_bf16_kernel<64><<<static_cast<int>(blocks), kPreThreads, 0, stream>>>(
-            static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.lse, a.delta,
-            a.lse2, a.N, a.n_pad, total);
-    else
-        bwd_pre_bf16_kernel<128><<<static_cast<int>(blocks), kPreThreads, 0, stream>>>(
-            static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.lse, a.delta,
-            a.lse2, a.N, a.n_pad, total);
+    kern<<<static_cast<int>(blocks), kPreThreads, 0, stream>>>(
+        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.lse, a.delta, a.lse2,
+        a.N, a.n_pad, total);
     return cudaGetLastError();
 }
 

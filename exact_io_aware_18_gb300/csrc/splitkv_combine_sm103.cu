@@ -11,7 +11,9 @@
 // One warp per query row: lanes take the split LSEs in strides and reduce the
 // max by shuffles, then each lane merges d/32 consecutive elements of O (16-
 // or 8-byte loads, so a warp reads each partial row in one 512- or 256-byte
-// transaction) and writes them as BF16.
+// transaction) and writes them as BF16.  The partials are read eight chunks
+// at a time, all loads first: one at a time, each chunk would wait for its own
+// L2 round trip.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -20,6 +22,7 @@ namespace fa {
 namespace {
 
 constexpr int kCombineThreads = 256;
+constexpr int kSplitBatch = 8;  // chunks whose partials are loaded together
 
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads)
@@ -39,20 +42,38 @@ __global__ void __launch_bounds__(kCombineThreads)
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[e] = 0.f;
         float wsum = 0.f;
-        for (int s = 0; s < n_splits; ++s) {
-            const float w = expf(lse_part[s * rows + row] - m);
-            wsum += w;
-            const float* src = o_part + (s * rows + row) * D + lane * E;
-            if constexpr (E == 4) {
-                const float4 x = *reinterpret_cast<const float4*>(src);
-                acc[0] = fmaf(w, x.x, acc[0]);
-                acc[1] = fmaf(w, x.y, acc[1]);
-                acc[2] = fmaf(w, x.z, acc[2]);
-                acc[3] = fmaf(w, x.w, acc[3]);
-            } else {
-                const float2 x = *reinterpret_cast<const float2*>(src);
-                acc[0] = fmaf(w, x.x, acc[0]);
-                acc[1] = fmaf(w, x.y, acc[1]);
+        for (int s0 = 0; s0 < n_splits; s0 += kSplitBatch) {
+            float lw[kSplitBatch];
+            float x[kSplitBatch][E];
+#pragma unroll
+            for (int u = 0; u < kSplitBatch; ++u) {
+                const int s = s0 + u;
+#pragma unroll
+                for (int e = 0; e < E; ++e) x[u][e] = 0.f;
+                lw[u] = -INFINITY;  // a missing chunk weighs exp(-inf) = 0
+                if (s < n_splits) {
+                    lw[u] = lse_part[s * rows + row];
+                    const float* src = o_part + (s * rows + row) * D + lane * E;
+                    if constexpr (E == 4) {
+                        const float4 v = *reinterpret_cast<const float4*>(src);
+                        x[u][0] = v.x;
+                        x[u][1] = v.y;
+                        x[u][2] = v.z;
+                        x[u][3] = v.w;
+                    } else {
+                        const float2 v = *reinterpret_cast<const float2*>(src);
+                        x[u][0] = v.x;
+                        x[u][1] = v.y;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kSplitBatch; ++u) {
+                if (s0 + u >= n_splits) break;
+                const float w = expf(lw[u] - m);
+                wsum += w;
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[u][e], acc[e]);
             }
         }
         const float inv = 1.f / wsum;

@@ -543,18 +543,75 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+CASES = ("fp8_quantize", "fp8_forward", "decode")
+
+
+def run_case(args):
+    """One next-row workload alone (for profiling): --warmup calls, then
+    --steps calls timed on the device; one JSON line with the mean time."""
+    import torch
+
+    import fa_inputs
+    import exact_io_aware_18_gb300 as fa
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(SEED)
+
+    def rnd(*shape):
+        return torch.randn(*shape, generator=gen, device=dev).to(torch.bfloat16)
+
+    scale = fa.default_scale(D)
+    if args.case in ("fp8_quantize", "fp8_forward"):
+        q, k, v = rnd(B, H, N, D), rnd(B, H, N, D), rnd(B, H, N, D)
+        signs = fa._lib._host_signs(fa_inputs.random_signs(SEED, D), D)
+        q8, qs = fa.fp8_quantize(q, signs, stream)
+        k8, ks = fa.fp8_quantize(k, signs, stream)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        if args.case == "fp8_quantize":
+            workload = f"rotation + E4M3 quantisation of one bf16 tensor B={B} H={H} N={N} d={D}"
+            fn = lambda: fa.fa_fp8_quantize(q, signs, q8, qs, stream)  # noqa: E731
+        else:
+            workload = f"FP8 forward B={B} H={H} N={N} d={D} causal (Q, K codes given)"
+            fn = lambda: fa.fa_fwd_fp8(q8, qs, k8, ks, v, o, lse, CAUSAL, scale, stream)  # noqa: E731
+    else:
+        db, dhq, dhkv, dnq, dnk = 4, 32, 8, 1, 16384
+        q, k, v = rnd(db, dhq, dnq, D), rnd(db, dhkv, dnk, D), rnd(db, dhkv, dnk, D)
+        o = torch.empty_like(q)
+        lse = torch.empty((db, dhq, dnq), dtype=torch.float32, device=dev)
+        ws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(db, dhq, dhkv, dnq, dnk, D) // 4 + 4,
+                         dtype=torch.float32, device=dev)
+        workload = f"split-KV decode B={db} Hq={dhq} Hkv={dhkv} Nq={dnq} Nk={dnk} d={D}"
+        fn = lambda: fa.fa_fwd_splitkv(q, k, v, o, lse, scale, 0, ws, stream)  # noqa: E731
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ms = _timed(torch, torch.cuda.current_stream(dev), fn, args.steps)
+    if fa.fa_device_status(clear=True) != fa.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait")
+    print(json.dumps({"case": args.case, "workload": workload, "ms": round(ms, 4),
+                      "steps": args.steps, "warmup": args.warmup}))
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--case", choices=CASES, default=None,
+                   help="run one next-row workload alone (for profiling) instead of the step")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.steps < 1:
         p.error("--steps must be at least 1")
-    if args.impl == "reference":
+    if args.case is not None:
+        run_case(args)
+    elif args.impl == "reference":
         if "--steps" not in (argv or sys.argv):
             args.steps = 5
         run_reference(args)

@@ -71,6 +71,33 @@ KERNEL_TRAFFIC = {
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def dist_env():
+    """(world, rank, local rank) from the launcher's environment (1, 0, 0 alone)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own batch (weak scaling: independent heads per rank)."""
+    return SEED + rank
+
+
+def max_over_ranks(torch, value: float, device, world: int) -> float:
+    """The largest of every rank's value, on every rank (the slowest rank sets
+    the job's time)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank: float, ms_per_step: float) -> float:
+    """Work of all ranks over the (max-over-ranks) time of one step."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def step_flops(b=B, h=H, n=N, d=D, causal=CAUSAL):
     fwd = 4.0 * b * h * n * n * d
     if causal:
@@ -293,9 +320,7 @@ def run_gpu(args):
     import torch
     import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = dist_env()
     if world > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
@@ -307,7 +332,7 @@ def run_gpu(args):
     import fa_inputs
 
     scale = fa.default_scale(D)
-    x = fa_inputs.attention_inputs(SEED + rank, B, H, N, D, "bf16")
+    x = fa_inputs.attention_inputs(rank_seed(rank), B, H, N, D, "bf16")
 
     def host_bf16(name):
         return torch.from_numpy(x[name + "_bits"].view(np.int16)).view(torch.bfloat16)
@@ -373,11 +398,7 @@ def run_gpu(args):
     t_wall1 = time.monotonic()
     if world > 1:
         dist.barrier()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(torch, start.elapsed_time(end), dev, world)
     if fa.fa_device_status(clear=True) != fa.FA_OK:
         raise RuntimeError("a kernel reported a timed-out wait in the timed region")
 
@@ -432,13 +453,15 @@ def run_gpu(args):
     e2e_steps = max(3, min(args.steps, 50))
     e2e_run(2)
     torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(s_main)
     e2e_run(e2e_steps)
     e1.record(s_main)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = max_over_ranks(torch, e0.elapsed_time(e1) / e2e_steps, dev, world)
     sampler.stop()
     next_rows = measure_next_rows(fa, torch, q, k, v, do, stream) if rank == 0 else None
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
@@ -451,7 +474,7 @@ def run_gpu(args):
 
     f_fwd, f_bwd = step_flops()
     ms_per_step = elapsed_ms / args.steps
-    value = world * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, f_fwd + f_bwd, ms_per_step)
     peaks, peak_kind = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     # Each kernel's own GEMM FLOPs per launch: the forward does 2 GEMMs per
@@ -501,7 +524,7 @@ def run_gpu(args):
                          "cores": cores, "kind": "oracle",
                          "sample": f"{n_heads} of {B * H} heads (whole heads, fwd+bwd), "
                                    f"{cpu_s:.1f} s"},
-        "e2e": {"value": round(world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12, 2),
+        "e2e": {"value": round(whole_job_tflops(world, f_fwd + f_bwd, e2e_ms), 2),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),
                 "copies": "own streams: step i+1's inputs in and step i-1's results out "
@@ -530,9 +553,8 @@ def run_gpu(args):
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    world, rank, _ = dist_env()
+    if rank != 0:  # under torchrun, rank 0 alone times the oracle
         return
     import fa_inputs
     cores = oracle_cores()

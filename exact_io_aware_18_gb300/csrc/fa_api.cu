@@ -112,9 +112,11 @@ int make_map_bf16(CUtensorMap* map, const void* ptr, int d, int N, long long BH)
 }
 
 // [B*H, N, d] E4M3 codes (bytes) viewed as (d, N, B*H) with one 128-row box
-// of d bytes: 128-byte swizzle at d = 128 (exactly its span), none at d = 64.
+// of d bytes: 128-byte swizzle at d = 128 (exactly its span); at d = 64 none
+// (the quantisation kernel's plain stores) or, for MMA operands, 64-byte.
 // Rows past N read as zero, the code of +0; stores past N are dropped.
-int make_map_u8(CUtensorMap* map, const void* ptr, int d, int N, long long BH) {
+int make_map_u8(CUtensorMap* map, const void* ptr, int d, int N, long long BH,
+                bool mma_operand = false) {
     EncodeFn enc;
     if (int rc = get_encode(&enc)) return rc;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
@@ -125,7 +127,8 @@ int make_map_u8(CUtensorMap* map, const void* ptr, int d, int N, long long BH) {
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                              : (mma_operand ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE),
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
@@ -432,14 +435,13 @@ int fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8, const float
     if (int rc = check_ptrs({q8, q_scale, k8, k_scale, v, o, lse})) return rc;
     if (int rc = check_shape(B, Hq, N, d, scale)) return rc;
     if (int rc = check_heads(Hq, Hkv)) return rc;
-    if (d != 128) return FA_ERR_UNSUPPORTED;
     unsigned int* status;
     if (int rc = status_ptr(&status)) return rc;
     const long long BH = static_cast<long long>(B) * Hq;
     const long long BHkv = static_cast<long long>(B) * Hkv;
     CUtensorMap tq, tk, tv, to;
-    if (int rc = make_map_u8(&tq, q8, d, N, BH)) return rc;
-    if (int rc = make_map_u8(&tk, k8, d, N, BHkv)) return rc;
+    if (int rc = make_map_u8(&tq, q8, d, N, BH, true)) return rc;
+    if (int rc = make_map_u8(&tk, k8, d, N, BHkv, true)) return rc;
     if (int rc = make_map_bf16(&tv, v, d, N, BHkv)) return rc;
     if (int rc = make_map_bf16(&to, o, d, N, BH)) return rc;
     unsigned int* work;

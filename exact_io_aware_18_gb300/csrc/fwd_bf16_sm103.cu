@@ -70,7 +70,8 @@ struct FwdCfg {
     static constexpr int KB = D / 64;                 // 64-column (128-byte) boxes per row
     static constexpr int BOX_BYTES = 128 * 64 * 2;    // one 128 x 64 bf16 box
     static constexpr int TILE_BYTES = KB * BOX_BYTES; // one 128 x D bf16 tile
-    // FP8: Q and K tiles are 128 x D E4M3 codes, one 128-byte-wide box (D = 128).
+    // FP8: Q and K tiles are 128 x D E4M3 codes, one box of D-byte rows
+    // (128-byte swizzle at D = 128, 64-byte swizzle at D = 64).
     static constexpr int QK_BYTES = FP8 ? 128 * D : TILE_BYTES;
     static constexpr int NS = (D == 128) ? 2 : 4;     // K/V ring depth
     static constexpr int QUEUE = 4;                   // claimed-tile queue depth
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(384, 1)
                     float* __restrict__ lse_part, const float* __restrict__ q_scale,
                     const float* __restrict__ k_scale) {
     using C = FwdCfg<D, FP8>;
-    static_assert(!(FP8 && (SPLIT || D != 128)), "the FP8 forward is built for d = 128, no split");
+    static_assert(!(FP8 && SPLIT), "the FP8 forward has no split mode");
     using Bar = FwdBars<C::NS, C::QUEUE>;
     static_assert(8 * Bar::COUNT + 8 <= C::BAR_BYTES, "barrier area");
     extern __shared__ uint8_t smem_raw[];
@@ -386,10 +387,16 @@ __global__ void __launch_bounds__(384, 1)
                                 constexpr uint32_t id_s8 = idesc_e4m3(128, 128);
                                 const uint32_t q_tile = s_q + (k & 1) * C::TILE_BYTES;
 #pragma unroll
-                                for (int kk = 0; kk < D / 32; ++kk)
-                                    mma_ss_f8(d_tmem, smem_desc_sw128(q_tile + kk * 32, 16, 1024),
-                                              smem_desc_sw128(k_tile + kk * 32, 16, 1024), id_s8,
-                                              kk > 0);
+                                for (int kk = 0; kk < D / 32; ++kk) {
+                                    if constexpr (D == 128)
+                                        mma_ss_f8(d_tmem, smem_desc_sw128(q_tile + kk * 32, 16, 1024),
+                                                  smem_desc_sw128(k_tile + kk * 32, 16, 1024),
+                                                  id_s8, kk > 0);
+                                    else
+                                        mma_ss_f8(d_tmem, smem_desc_sw64(q_tile + kk * 32, 512),
+                                                  smem_desc_sw64(k_tile + kk * 32, 512), id_s8,
+                                                  kk > 0);
+                                }
                             } else {
 #pragma unroll
                                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -693,7 +700,8 @@ cudaError_t launch_fwd_splitkv_bf16(const FwdArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
-    if (a.d != 128) return cudaErrorInvalidValue;
+    if (a.d == 64) return a.causal ? launch_fwd_t<64, true, false, true>(a, stream)
+                                   : launch_fwd_t<64, false, false, true>(a, stream);
     return a.causal ? launch_fwd_t<128, true, false, true>(a, stream)
                     : launch_fwd_t<128, false, false, true>(a, stream);
 }

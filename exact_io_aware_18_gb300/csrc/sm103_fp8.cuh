@@ -26,4 +26,17 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// Shared-memory matrix descriptor for a 64-byte-swizzled K-major operand:
+// rows of 64 bytes (64 E4M3 codes), 512-byte atoms of 8 rows whose 16-byte
+// chunks are XOR-ed with the address bits above them, every atom 512-byte
+// aligned.  sbo is the byte stride between 8-row groups (512 for a dense
+// tile); the leading offset is not used.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t sbo_bytes) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>(1u) << 16) |                             // leading offset (unused)
+           (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) |
+           (1ull << 46) |  // descriptor version for tcgen05
+           (4ull << 61);   // 64-byte swizzle
+}
+
 }  // namespace fa

@@ -189,7 +189,7 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
  * fa_fwd_fp8: attention with S = (Q R)(K R)^T computed from the codes on the
  * FP8 tensor cores (FP32 accumulation) and multiplied by the Q and K tile
  * scales; P V in BF16 as in fa_fwd.  Output O (bf16 [B,Hq,N,d]) and LSE
- * (float [B,Hq,N]) as fa_fwd_gqa.  d must be 128 (FA_ERR_UNSUPPORTED).
+ * (float [B,Hq,N]) as fa_fwd_gqa.  d is 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
  *   q8, q_scale : fa_fp8_quantize of q [B,Hq,N,d] (BH = B*Hq).
  *   k8, k_scale : fa_fp8_quantize of k [B,Hkv,N,d] with the same signs.
  *   v           : bf16 [B,Hkv,N,d], not rotated.

@@ -167,7 +167,7 @@ def test_fp8_argument_checks_before_launch(fa):
     def fwd(B=1, Hq=4, Hkv=2, N=256, d=128, scale=0.125, ptrs=None):
         ptrs = ptrs or [P] * 7
         return lib.fa_fwd_fp8(*ptrs, B, Hq, Hkv, N, d, 1, scale, None)
-    assert fwd(d=64) == fa.FA_ERR_UNSUPPORTED            # the FP8 forward is built for d = 128
+    assert fwd(d=96) == fa.FA_ERR_UNSUPPORTED            # head dimension 64 or 128
     assert fwd(Hkv=3) == fa.FA_ERR_INVALID_ARG           # 3 does not divide 4
     assert fwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert fwd(ptrs=[P, 0, P, P, P, P, P]) == fa.FA_ERR_INVALID_ARG   # no Q scales

@@ -93,6 +93,8 @@ CASES = [  # B, Hq, Hkv, N, d, causal
     (1, 4, 2, 257, 128, True),     # grouped-query, ragged last tile
     (1, 2, 1, 1000, 128, False),   # multi-query, several key tiles
     (1, 1, 1, 1, 128, True),       # one query, one key
+    (1, 2, 2, 300, 64, True),      # d = 64: 64-byte rows of codes
+    (2, 4, 2, 513, 64, False),     # d = 64, grouped-query, ragged last tile
 ]
 
 

@@ -430,31 +430,29 @@ __global__ void __launch_bounds__(384, 1)
         float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);  // [2][2][128] maxima, [2][128] sums
         int g = 0;             // tile counter across this CTA's Q tiles
         int pending_qb = -1;   // store thread: Q buffer whose O store may still be reading it
-        for (int k = 0;; ++k) {
-            // All eight warps agree on the tile (or on stopping) before using it.
+        // Tile k from the queue; all eight warps agree on it (or on stopping).
+        auto take = [&](int k) -> int {
             const int slot = k % C::QUEUE;
             const bool okq = __all_sync(
                 0xffffffffu, mbar_wait(bar(Bar::ITEM_FULL + slot), (k / C::QUEUE) & 1, wc));
             const int item = okq ? items[slot] : -1;
             __syncwarp();
             if (okq && lane == 0) mbar_arrive(bar(Bar::ITEM_EMPTY + slot));
-            if (!named_bar_and(5, 256, okq && item >= 0)) break;
-            const Work w = work_of(item);
-            const int qt = w.qt;
-            const int bh = w.bh;
-            const int grow = qt * C::BM + row;  // query index inside the head
+            return named_bar_and(5, 256, okq && item >= 0) ? item : -1;
+        };
+        // Q of tile k into TMEM as BF16 pairs (the A operand of S = Q K^T):
+        // this thread's row, elements [h d/2, (h+1) d/2), read from the
+        // swizzled tile, once the previous tile's S MMAs have finished with it.
+        // (FP8: the S MMAs read Q's codes from shared memory; nothing to copy.)
+        auto copy_q = [&](int k) -> bool {
+            if constexpr (FP8) return true;
             const int qb = k & 1;
-            const uint32_t q_buf = C::OFF_Q + qb * C::TILE_BYTES;
-
-            // Q into TMEM as BF16 pairs (the A operand of S = Q K^T): this
-            // thread's row, elements [h d/2, (h+1) d/2), read from the swizzled
-            // tile, once the previous tile's S MMAs have finished with it.
-            // (FP8: the S MMAs read Q's codes from shared memory; nothing to copy.)
-            bool ok = FP8 || __all_sync(0xffffffffu,
-                                        mbar_wait(bar(Bar::Q_FULL + qb), (k >> 1) & 1, wc) &&
-                                            (k == 0 || mbar_wait(bar(Bar::QT_EMPTY), (k - 1) & 1, wc)));
-            if (!FP8 && ok) {
+            const bool ok = __all_sync(
+                0xffffffffu, mbar_wait(bar(Bar::Q_FULL + qb), (k >> 1) & 1, wc) &&
+                                 (k == 0 || mbar_wait(bar(Bar::QT_EMPTY), (k - 1) & 1, wc)));
+            if (ok) {
                 tc_fence_after();
+                const uint32_t q_buf = C::OFF_Q + qb * C::TILE_BYTES;
                 uint32_t qw[D / 4];
 #pragma unroll
                 for (int c = 0; c < D / 16; ++c) {
@@ -474,6 +472,18 @@ __global__ void __launch_bounds__(384, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(Bar::QT_FULL));
             }
+            return ok;
+        };
+        int item = take(0);
+        bool q_ok = item >= 0 && copy_q(0);
+        for (int k = 0; item >= 0; ++k) {
+            const Work w = work_of(item);
+            const int qt = w.qt;
+            const int bh = w.bh;
+            const int grow = qt * C::BM + row;  // query index inside the head
+            const int qb = k & 1;
+            const uint32_t q_buf = C::OFF_Q + qb * C::TILE_BYTES;
+            bool ok = q_ok;
 
             float m_run = -INFINITY;  // running max, base-2 units of scale * S
             float l_run = 0.f;        // this half's running sum of 2^(x - m_run)
@@ -575,6 +585,11 @@ __global__ void __launch_bounds__(384, 1)
                     pending_qb = -1;
                 }
             }
+            // The next tile's Q goes into TMEM now, before this tile's
+            // epilogue, so that its first score MMAs run meanwhile (its S
+            // buffers are free, and its first P V waits for its own P).
+            const int next = take(k + 1);
+            q_ok = next >= 0 && copy_q(k + 1);
             // Both warps of the pair reach this barrier after the same iteration.
             xch[512 + h * 128 + row] = l_run;
             ok = named_bar_and(pair_bar, 64, ok);
@@ -647,6 +662,7 @@ __global__ void __launch_bounds__(384, 1)
                 bulk_commit();
                 pending_qb = qb;
             }
+            item = next;
         }
         if (threadIdx.x == kStoreThread && pending_qb >= 0) bulk_wait_read_all();
     }

@@ -40,9 +40,11 @@
 //               P buffer once PV_{j-1} has read it, and rescale its d/2
 //               columns of the O accumulator only when the max grew by more
 //               than 2^8 (the final O / l and LSE use the same stale max, so
-//               the result is unchanged).  Epilogue: the two halves of l are
-//               summed, O / l goes to BF16 into the tile's Q buffer and out by
-//               TMA store; LSE = ln 2 * (m + log2 l).
+//               the result is unchanged).  After a Q tile's last key tile
+//               the next Q tile's Q goes into TMEM first, so that its first
+//               score MMAs run during this tile's epilogue: the two halves of
+//               l are summed, O / l goes to BF16 into the tile's Q buffer and
+//               out by TMA store; LSE = ln 2 * (m + log2 l).
 // Warpgroup 0 (warps 0-3) hands registers to the softmax warpgroups, which
 // hold a row half of scores, probabilities and O in flight.
 //

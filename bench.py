@@ -60,8 +60,8 @@ def kernel_src_sha256(name: str) -> str:
 
 KERNEL_TRAFFIC = {
     # profiles/kernels_training_step_b8_h16_n2048_d128_causal.md (ncu --set full)
-    "fwd_bf16": {"bytes": 201501440 + 47808000,
-                 "src_sha256": "a87f7316cb4edd5c80c3d57c5089f5275b01349bb1da2240c9045b39b7ef289d"},
+    "fwd_bf16": {"bytes": 201417984 + 48139776,
+                 "src_sha256": "c6777adbbbc70cb68ac9a2386394915d33d1f274f201c22d612fd1bfc03b91a1"},
     "bwd_dkdv_bf16": {"bytes": 270640384 + 218950656,
                       "src_sha256": "bf2c213825688402631586a67f108ad1d2b8d8bbbd0ba2885fd9eb8c3a67a479"},
     "bwd_dq_bf16": {"bytes": 270698496 + 108191744,

@@ -260,13 +260,33 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
 
 // Split-KV plan: the key tiles are cut into chunks of chunk_tiles; n_splits
 // chunks, none empty.  The query rows of a K/V head's group (g query heads x
-// Nq queries, contiguous in memory) form its Q tiles; requested <= 0 asks for
-// enough chunks that the (K/V head, Q tile, chunk) items fill every SM about
-// four times, so that the last partial wave is short.
+// Nq queries, contiguous in memory) form its Q tiles; requested <= 0 lets the
+// library choose.  Its choice minimises the time of the busiest SM, modelled
+// as waves x (chunk_tiles + 2): waves = ceil(items / SMs) for the (K/V head,
+// Q tile, chunk) items, and about two tiles' worth of work per item besides
+// its key tiles (Q copy, epilogue, partial store).  A part-filled last wave
+// costs a whole one, so the count that fills whole waves wins; on a tie the
+// fewer chunks (less to merge).
 struct SplitPlan {
     int n_splits;
     int chunk_tiles;
 };
+
+long long auto_splits(long long kv_tiles, long long q_items, long long sms) {
+    long long best = 1, best_cost = -1;
+    for (long long n = 1; n <= kv_tiles && n <= 256; ++n) {
+        const long long chunk = (kv_tiles + n - 1) / n;
+        const long long used = (kv_tiles + chunk - 1) / chunk;  // chunks actually made
+        if (used != n) continue;
+        const long long waves = (q_items * n + sms - 1) / sms;
+        const long long cost = waves * (chunk + 2);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = n;
+        }
+    }
+    return best;
+}
 
 int split_plan(int B, int Hq, int Hkv, int Nq, int Nk, int requested, SplitPlan* out) {
     const long long kv_tiles = (static_cast<long long>(Nk) + 127) / 128;
@@ -277,7 +297,7 @@ int split_plan(int B, int Hq, int Hkv, int Nq, int Nk, int requested, SplitPlan*
         unsigned int* unused;
         int sms = 0;
         if (int rc = work_slot(&unused, &sms)) return rc;
-        want = (4LL * sms + q_items - 1) / q_items;
+        want = auto_splits(kv_tiles, q_items, sms > 0 ? sms : 1);
     }
     if (want < 1) want = 1;
     if (want > kv_tiles) want = kv_tiles;

@@ -152,9 +152,10 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
  * The g = Hq / Hkv query heads of a K/V head share its tiles: their g * Nq
  * query rows (contiguous in q) are computed together, 128 rows at a time,
  * so each K/V tile is read once per group.
- * n_splits <= 0 lets the library choose (enough chunks to fill every SM
- * about four times); the count actually used never leaves a chunk empty and
- * is at most the number of 128-key tiles.
+ * n_splits <= 0 lets the library choose: the count that minimises waves x
+ * (key tiles per chunk + 2) for the (K/V head, 128-query tile, chunk) items
+ * over the SMs, so that the items fill whole waves; the count actually used
+ * never leaves a chunk empty and is at most the number of 128-key tiles.
  * workspace : device buffer of at least
  *             fa_fwd_splitkv_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, n_splits)
  *             bytes, 16-byte aligned, or NULL: the library then allocates and

@@ -42,6 +42,7 @@ _SIGNATURES = {
     "fa_bwd_f32": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _sz, _vp], _i),
     "fa_error_string": ([_i], ctypes.c_char_p),
     "fa_device_status": ([_i], _i),
+    "fa_last_device_status": ([], _i),
     "fa_set_wait_timeout_ns": ([ctypes.c_ulonglong], None),
     "fa_selftest_wait_timeout": ([ctypes.c_ulonglong, _vp], _i),
     "fa_bwd_noalloc": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp], _i),
@@ -353,6 +354,10 @@ def fa_bwd_f32(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, work
 
 def fa_device_status(clear: bool = False) -> int:
     return int(load().fa_device_status(int(bool(clear))))
+
+
+def fa_last_device_status() -> int:
+    return int(load().fa_last_device_status())
 
 
 def fa_set_wait_timeout_ns(ns: int) -> None:

@@ -346,6 +346,8 @@ int fa_device_status(int clear) {
     return word ? FA_ERR_CUDA : FA_OK;  // bit 1: a kernel found its shared memory misplaced
 }
 
+int fa_last_device_status(void) { return fa_device_status(0); }
+
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, int causal, float scale, void* stream) {
     return fwd_impl(q, k, v, o, lse, B, H, H, N, d, causal, scale, stream);

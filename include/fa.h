@@ -243,6 +243,9 @@ const char* fa_error_string(int status);
  * clear != 0 resets the word. */
 int fa_device_status(int clear);
 
+/* The same check without clearing the word: fa_device_status(0). */
+int fa_last_device_status(void);
+
 /* Upper bound, in nanoseconds, on any single wait inside a kernel launched
  * after this call (default 4e9).  Values below 1e6 are raised to 1e6. */
 void fa_set_wait_timeout_ns(unsigned long long ns);

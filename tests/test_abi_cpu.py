@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("fa_fwd", "fa_bwd", "fa_fwd_f32", "fa_bwd_f32", "fa_bwd_workspace_bytes",
                  "fa_error_string", "fa_device_status", "fa_bwd_preprocess", "fa_bwd_dkdv",
-                 "fa_bwd_dq", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fp8_quantize", "fa_fwd_fp8"):
+                 "fa_bwd_dq", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fp8_quantize", "fa_fwd_fp8",
+                 "fa_last_device_status"):
         assert must in names
 
 

@@ -281,26 +281,30 @@ def measure_next_rows(fa, torch, q, k, v, do, stream, iters=20):
                      iters)
     # per tensor: BF16 read, E4M3 codes and one FP32 scale per 128-row tile written
     quant_bytes = B * H * N * D * 3 + B * H * ((N + 127) // 128) * 4
-    # The forward alone on the long-sequence workloads whose tensor-core
-    # fraction the targets are stated on (seeded device inputs).
+    # The forward alone on the forward-only workloads (the long-sequence ones
+    # carry the tensor-core target), seeded device inputs.
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     fwd_rows = {}
-    for name, (fb, fh, fn) in (("B4_H16_N4096_causal", (4, 16, 4096)),
-                               ("B1_H16_N32768_causal", (1, 16, 32768))):
-        fq, fk, fv = rnd(fb, fh, fn, D), rnd(fb, fh, fn, D), rnd(fb, fh, fn, D)
+    for name, (fb, fh, fn, fd, fc) in (("B2_H8_N1024_d64", (2, 8, 1024, 64, False)),
+                                       ("B4_H16_N4096_causal", (4, 16, 4096, 128, True)),
+                                       ("B1_H16_N32768_causal", (1, 16, 32768, 128, True))):
+        fq, fk, fv = rnd(fb, fh, fn, fd), rnd(fb, fh, fn, fd), rnd(fb, fh, fn, fd)
         fo = torch.empty_like(fq)
         flse = torch.empty((fb, fh, fn), dtype=torch.float32, device=q.device)
-        f_ms = _timed(torch, stream, lambda: fa.fa_fwd(fq, fk, fv, fo, flse, True, scale, stream),
+        fs = fa.default_scale(fd)
+        f_ms = _timed(torch, stream, lambda: fa.fa_fwd(fq, fk, fv, fo, flse, fc, fs, stream),
                       max(3, iters // 2))
-        f_tf = step_flops(fb, fh, fn, D, True)[0] / (f_ms * 1e-3) / 1e12
+        f_tf = step_flops(fb, fh, fn, fd, fc)[0] / (f_ms * 1e-3) / 1e12
         fwd_rows[name] = {"ms": round(f_ms, 4), "tflops": round(f_tf, 2),
-                          "frac_of_burst_peak": round(f_tf / burst, 4)}
+                          "frac_of_burst_peak": round(f_tf / burst, 4),
+                          "frac_of_nominal_2250": round(f_tf / 2250.0, 4)}
         del fq, fk, fv, fo, flse
     if fa.fa_device_status(clear=True) != fa.FA_OK:
         raise RuntimeError("a kernel reported a timed-out wait in the next-row measurements")
     return {
-        "forward_long_sequences": dict(fwd_rows, peak="bf16_tflops (burst, measured)",
-                                       flops="4 B H N^2 d, causal halved"),
+        "forward_workloads": dict(fwd_rows, peak="bf16_tflops (burst, measured); "
+                                  "nominal dense BF16 2250 TFLOP/s",
+                                  flops="4 B H N^2 d, causal halved"),
         "fp8_forward": {
             "workload": f"B={B} H={H} N={N} d={D} causal: Q, K rotated by a random-sign Hadamard "
                         "transform and quantised to E4M3 per 128-row tile; S from the codes on "

@@ -64,8 +64,8 @@ KERNEL_TRAFFIC = {
                  "src_sha256": "c6777adbbbc70cb68ac9a2386394915d33d1f274f201c22d612fd1bfc03b91a1"},
     "bwd_dkdv_bf16": {"bytes": 270640384 + 218950656,
                       "src_sha256": "bf2c213825688402631586a67f108ad1d2b8d8bbbd0ba2885fd9eb8c3a67a479"},
-    "bwd_dq_bf16": {"bytes": 270698496 + 108191744,
-                    "src_sha256": "168b9eec1cd34cabe7ec22a9c52ca1cd6f4b2ee7d26161b1b958d7cfc46c0230"},
+    "bwd_dq_bf16": {"bytes": 336733184 + 112622592,
+                    "src_sha256": "1568fb97e527eaaabadbfe08648f998e2bbdac58813221b7328bd414e79656ab"},
 }
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps
@@ -378,15 +378,13 @@ def run_gpu(args):
         fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream)
         if ev is not None:
             ev[1].record(stream)
-        fa.fa_bwd_preprocess(o, do, lse, delta, lse2, stream)
+        # dQ with the first backward step fused (it writes D and LSE2), then dK/dV.
+        fa.fa_bwd_dq_preprocess(q, k, v, o, do, lse, delta, lse2, dq, CAUSAL, scale, stream)
         if ev is not None:
             ev[2].record(stream)
         fa.fa_bwd_dkdv(q, k, v, do, delta, lse2, dk, dv, CAUSAL, scale, stream)
         if ev is not None:
             ev[3].record(stream)
-        fa.fa_bwd_dq(q, k, v, do, delta, lse2, dq, CAUSAL, scale, stream)
-        if ev is not None:
-            ev[4].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -405,7 +403,7 @@ def run_gpu(args):
     sampler.start()
     time.sleep(0.3)
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -425,9 +423,8 @@ def run_gpu(args):
         raise RuntimeError("a kernel reported a timed-out wait in the timed region")
 
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
-    pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+    dq_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
     dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in events)
-    dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in events)
 
     # End to end through the public calls: every step copies its inputs in
     # from pinned host memory and its results (O, LSE, dQ, dK, dV) back.  As
@@ -522,8 +519,6 @@ def run_gpu(args):
     n_heads = max(1, min(B * H, cores))
     cpu_s, cpu_flops = oracle_step_sample(x, n_heads)
 
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    pre_bytes = 2 * B * H * N * D * 2 + B * H * N * 4 + 2 * B * H * n_pad * 4
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -551,19 +546,17 @@ def run_gpu(args):
                 "ms_per_step": round(e2e_ms, 4),
                 "copies": "own streams: step i+1's inputs in and step i-1's results out "
                           "while step i computes (two device buffer sets)"},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "kernels": {
             "fwd": {"ms": round(fwd_ms, 4), "tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
                     "frac_of_peak": round(f_fwd / (fwd_ms * 1e-3) / 1e12 / peak, 4)},
-            "bwd_preprocess": {"ms": round(pre_ms, 4),
-                               "gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
-                               "frac_of_hbm": round(pre_bytes / (pre_ms * 1e-3) / 1e9 / hbm, 4)},
+            "bwd_dq": {"ms": round(dq_ms, 4),
+                       "tflops": round(kern_flops["bwd_dq_bf16"] / (dq_ms * 1e-3) / 1e12, 2),
+                       "includes": "the first backward step: D = rowsum(dO o O), LSE log2(e)"},
             "bwd_dkdv": {"ms": round(dkdv_ms, 4),
                          "tflops": round(kern_flops["bwd_dkdv_bf16"] / (dkdv_ms * 1e-3) / 1e12, 2)},
-            "bwd_dq": {"ms": round(dq_ms, 4),
-                       "tflops": round(kern_flops["bwd_dq_bf16"] / (dq_ms * 1e-3) / 1e12, 2)},
-            "bwd_total_tflops": round(f_bwd / ((pre_ms + dkdv_ms + dq_ms) * 1e-3) / 1e12, 2),
+            "bwd_total_tflops": round(f_bwd / ((dkdv_ms + dq_ms) * 1e-3) / 1e12, 2),
         },
         "next_rows": next_rows,
     }

@@ -18,16 +18,16 @@ import torch
 from . import _lib
 from ._lib import (FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT, FA_ERR_INVALID_ARG, FA_ERR_MISALIGNED,
                    FA_ERR_NO_MEMORY, FA_ERR_UNSUPPORTED, FA_OK, FaError, error_string, fa_bwd,
-                   fa_bwd_dkdv, fa_bwd_dq, fa_bwd_f32, fa_bwd_gqa, fa_bwd_noalloc,
-                   fa_bwd_preprocess, fa_bwd_workspace_bytes, fa_device_status, fa_fp8_quantize,
-                   fa_fwd, fa_fwd_f32, fa_fwd_fp8, fa_fwd_gqa, fa_fwd_splitkv,
-                   fa_fwd_splitkv_workspace_bytes,
-                   fa_selftest_wait_timeout,
+                   fa_bwd_dkdv, fa_bwd_dq, fa_bwd_dq_preprocess, fa_bwd_f32, fa_bwd_gqa,
+                   fa_bwd_noalloc, fa_bwd_preprocess, fa_bwd_workspace_bytes, fa_device_status,
+                   fa_fp8_quantize, fa_fwd, fa_fwd_f32, fa_fwd_fp8, fa_fwd_gqa, fa_fwd_splitkv,
+                   fa_fwd_splitkv_workspace_bytes, fa_selftest_wait_timeout,
                    fa_set_wait_timeout_ns, lib_path, load)
 
 __all__ = [
     "attention_fwd", "attention_bwd", "fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv",
-    "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_splitkv",
+    "fa_bwd_dq", "fa_bwd_dq_preprocess", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa",
+    "fa_fwd_splitkv",
     "fa_fwd_splitkv_workspace_bytes", "attention_decode", "fa_fp8_quantize", "fa_fwd_fp8",
     "fp8_quantize", "attention_fwd_fp8",
     "fa_bwd_workspace_bytes", "fa_fwd_f32", "fa_bwd_f32", "fa_device_status",

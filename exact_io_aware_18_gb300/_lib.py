@@ -38,6 +38,7 @@ _SIGNATURES = {
     "fa_bwd_preprocess": ([_vp] * 5 + [_i, _i, _i, _i, _vp], _i),
     "fa_bwd_dkdv": ([_vp] * 8 + [_i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_bwd_dq": ([_vp] * 7 + [_i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_bwd_dq_preprocess": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_fwd_f32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_bwd_f32": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _sz, _vp], _i),
     "fa_error_string": ([_i], ctypes.c_char_p),
@@ -285,7 +286,7 @@ def _bwd_step_inputs(q, k, v, do, delta_ws, lse2_ws):
 
 def fa_bwd_dkdv(q, k, v, do, delta_ws, lse2_ws, dk, dv, causal: bool, scale: float,
                 stream=None) -> None:
-    """dK and dV, after fa_bwd_preprocess."""
+    """dK and dV, after fa_bwd_preprocess or fa_bwd_dq_preprocess."""
     B, H, N, d = _bwd_step_inputs(q, k, v, do, delta_ws, lse2_ws)
     for name, t in (("dk", dk), ("dv", dv)):
         _expect(t, name, torch.float32, (B, H, N, d))
@@ -302,6 +303,20 @@ def fa_bwd_dq(q, k, v, do, delta_ws, lse2_ws, dq, causal: bool, scale: float,
     _check(load().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(delta_ws), _ptr(lse2_ws),
                             _ptr(dq), B, H, N, d, int(bool(causal)), float(scale),
                             _stream(stream)), "fa_bwd_dq")
+
+
+def fa_bwd_dq_preprocess(q, k, v, o, do, lse, delta_ws, lse2_ws, dq, causal: bool,
+                         scale: float, stream=None) -> None:
+    """dQ with the first backward step fused: also writes delta_ws and lse2_ws
+    (as fa_bwd_preprocess does) for fa_bwd_dkdv, which runs after it."""
+    B, H, N, d = _bwd_step_inputs(q, k, v, do, delta_ws, lse2_ws)
+    _expect(o, "o", torch.bfloat16, (B, H, N, d))
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    _expect(dq, "dq", torch.float32, (B, H, N, d))
+    _check(load().fa_bwd_dq_preprocess(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                       _ptr(delta_ws), _ptr(lse2_ws), _ptr(dq), B, H, N, d,
+                                       int(bool(causal)), float(scale), _stream(stream)),
+           "fa_bwd_dq_preprocess")
 
 
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float,

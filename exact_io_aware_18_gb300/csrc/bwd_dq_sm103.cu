@@ -27,7 +27,12 @@
 //               registers.  S is double buffered and dP is released early, so
 //               both operands of tile j+1 are ready when the math of tile j
 //               ends.
-//   warps 2..9  thread (r, h) owns query row r (TMEM lane r) and key half h:
+//   warps 2..9  thread (r, h) owns query row r (TMEM lane r) and key half h.
+//               Given O and LSE, they first do the backward's first step for
+//               their rows (D_r = sum_c dO_rc O_rc from dO in shared memory
+//               and O from global memory, LSE2_r = LSE_r log2 e) and write
+//               D and LSE2 out for the dK/dV kernel; else they read both.
+//               Per key tile:
 //               P' = exp2(S * scale*log2e - LSE2_r + log2 scale) = scale P,
 //               dS' = P' o (dP - D_r) = scale dS, BF16, written over the first
 //               32 of its own 64 S columns.  At the end: the dQ row half out
@@ -58,7 +63,8 @@ struct DqCfg {
     static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_V + NSV * TILE_BYTES;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int LAYOUT_BYTES = OFF_BAR + BAR_BYTES;
+    static constexpr int OFF_XCH = OFF_BAR + BAR_BYTES;  // float [2][128]: D halves
+    static constexpr int LAYOUT_BYTES = OFF_XCH + 2 * BM * 4;
     static constexpr int SMEM_BYTES =
         (LAYOUT_BYTES + 1024 <= kMaxDynSmem) ? LAYOUT_BYTES + 1024 : kMaxDynSmem;
     static_assert(LAYOUT_BYTES <= kMaxDynSmem, "dQ tiles do not fit in shared memory");
@@ -94,7 +100,8 @@ __global__ void __launch_bounds__(384, 1)
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dq,
-                       const float* __restrict__ delta, const float* __restrict__ lse2, int N, int n_pad, int BH,
+                       const uint4* __restrict__ o, const float* __restrict__ lse,
+                       float* __restrict__ delta, float* __restrict__ lse2, int N, int n_pad, int BH,
                        int Hq, int n_rep, int n_tiles, int group,
                        float scale, float scale_log2, unsigned int* status,
                        unsigned long long timeout_ns) {
@@ -281,11 +288,78 @@ __global__ void __launch_bounds__(384, 1)
         const int qglob = qt * C::BM + r;    // query index inside the head
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const long long voff = static_cast<long long>(bh) * n_pad + qt * C::BM + r;
-        // +inf on padding rows, so P = 0 there; log2(scale) folds scale into P.
-        const float neg_l2 = log2f(scale) - lse2[voff];
-        const float d_r = delta[voff];
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
+        float d_r, l2_r;  // D_r and LSE_r log2(e); 0 and +inf on padding rows
+        if (o != nullptr) {
+            // The first backward step, fused: D_r = sum_c dO_rc O_rc with dO
+            // from the shared tile and O from global memory, LSE2_r from LSE.
+            // Loads are warp-wide: lane l takes 16-byte chunk l % CH of row
+            // i RPI + l / CH of this warp's 32 rows, so each load instruction
+            // reads whole row halves; the chunk sums meet by shuffles, and the
+            // two halves of a row through shared memory.
+            constexpr int CH = D / 16;   // 16-byte chunks in half a row
+            constexpr int RPI = 32 / CH;
+            const int c = lane % CH;
+            const int col0 = h * (D / 2);
+            const bool real = qglob < N;
+            // LSE goes out with the O loads: issued after the exchange, its
+            // latency would delay the first tile.
+            const float lse_r = real ? lse[static_cast<long long>(bh) * N + qglob] : 0.f;
+            uint4 ov[CH];
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+                const int row = qt * C::BM + wq * 32 + i * RPI + lane / CH;
+                ov[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (row < N)
+                    ov[i] = o[((static_cast<long long>(bh) * N + row) * D + col0) / 8 + c];
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::QD_FULL), 0, wc));
+            float part[CH];
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+                const int rt = wq * 32 + i * RPI + lane / CH;  // row inside the tile
+                const int chunk = (col0 % 64) / 8 + c;         // 16-byte chunk inside the box
+                const uint4 dv = *reinterpret_cast<const uint4*>(
+                    smem + C::OFF_DO + (col0 / 64) * C::BOX_BYTES + rt * 128 +
+                    ((chunk ^ (rt & 7)) << 4));
+                const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ov[i]);
+                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+                float acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = __bfloat1622float2(a2[e]);
+                    const float2 y = __bfloat1622float2(b2[e]);
+                    acc = fmaf(x.x, y.x, acc);
+                    acc = fmaf(x.y, y.y, acc);
+                }
+#pragma unroll
+                for (int off = CH / 2; off > 0; off >>= 1)
+                    acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                part[i] = acc;
+            }
+            // Lane L owns row L: load i = L / RPI, any lane of group L % RPI.
+            float mine = 0.f;
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+                const float t = __shfl_sync(0xffffffffu, part[i], (lane % RPI) * CH);
+                if (i == lane / RPI) mine = t;
+            }
+            float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+            xch[h * C::BM + r] = mine;
+            ok = named_bar_and(1, 32 * C::COMPUTE_WARPS, ok);
+            d_r = real ? xch[r] + xch[C::BM + r] : 0.f;
+            l2_r = real ? lse_r * 1.4426950408889634f : INFINITY;
+            if (h == 0) {
+                delta[voff] = d_r;
+                lse2[voff] = l2_r;
+            }
+        } else {
+            d_r = delta[voff];
+            l2_r = lse2[voff];
+        }
+        // P = 0 on padding rows (l2_r = +inf); log2(scale) folds scale into P.
+        const float neg_l2 = log2f(scale) - l2_r;
+        for (int j = 0; ok && j < n_kv; ++j) {
             const uint32_t t_s = t_lane + ((j & 1) ? C::COL_S1 : C::COL_S0) + 64 * h;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_FULL + (j & 1)), (j >> 1) & 1, wc) &&
                                              mbar_wait(bar(Bar::DP_FULL), j & 1, wc));
@@ -381,7 +455,8 @@ cudaError_t launch_t(const DqArgs& a, cudaStream_t stream) {
     if (group < 1) group = 1;
     dim3 grid(n_tiles, a.H, a.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, a.delta, a.lse2, a.N, a.n_pad, a.B * a.H,
+        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, static_cast<const uint4*>(a.o), a.lse,
+        a.delta, a.lse2, a.N, a.n_pad, a.B * a.H,
         a.H, a.H / a.Hkv, n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
     return cudaGetLastError();
 }

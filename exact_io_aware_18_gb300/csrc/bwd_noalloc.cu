@@ -16,10 +16,11 @@
 // Because of that one-time look-up, make the first call on a device before any
 // stream capture begins.
 //
-// Every call shares the one array and leaves its contents behind.  The
-// preprocess step rewrites every entry it reads later (padding rows included),
-// so nothing needs clearing between calls; but two calls that run on the GPU
-// at the same time (on different streams, say) would race on the array.
+// Every call shares the one array and leaves its contents behind.  The dQ
+// step (with the first step fused) rewrites every entry that dK/dV reads
+// later (padding rows included), so nothing needs clearing between calls;
+// but two calls that run on the GPU at the same time (on different streams,
+// say) would race on the array.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -73,10 +74,9 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
     const size_t half = need / (2 * sizeof(float));  // B*H*roundup(N,128) floats
     float* delta = scratch;
     float* lse2 = scratch + half;
-    int rc = fa_bwd_preprocess(o, do_, lse, delta, lse2, B, H, N, d, stream);
+    int rc = fa_bwd_dq_preprocess(q, k, v, o, do_, lse, delta, lse2, dq, B, H, N, d, causal,
+                                  scale, stream);
     if (rc == FA_OK)
         rc = fa_bwd_dkdv(q, k, v, do_, delta, lse2, dk, dv, B, H, N, d, causal, scale, stream);
-    if (rc == FA_OK)
-        rc = fa_bwd_dq(q, k, v, do_, delta, lse2, dq, B, H, N, d, causal, scale, stream);
     return rc;
 }

@@ -231,10 +231,15 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* do_,
     return launch_rc(fa::launch_bwd_dkdv_bf16(a, static_cast<cudaStream_t>(stream)));
 }
 
-int dq_impl(const void* q, const void* k, const void* v, const void* do_, const float* delta_ws,
-            const float* lse2_ws, float* dq, int B, int Hq, int Hkv, int N, int d, int causal,
-            float scale, void* stream) {
+// o and lse both null: dQ alone, from delta_ws / lse2_ws as the first step
+// wrote them.  Both set: the kernel also does the first step and writes them.
+int dq_impl(const void* q, const void* k, const void* v, const void* o, const void* do_,
+            const float* lse, float* delta_ws, float* lse2_ws, float* dq, int B, int Hq,
+            int Hkv, int N, int d, int causal, float scale, void* stream) {
     if (int rc = check_ptrs({q, k, v, do_, delta_ws, lse2_ws, dq})) return rc;
+    if ((o == nullptr) != (lse == nullptr)) return FA_ERR_INVALID_ARG;
+    if (o)
+        if (int rc = check_ptrs({o, lse})) return rc;
     if (int rc = check_shape(B, Hq, N, d, scale)) return rc;
     if (int rc = check_heads(Hq, Hkv)) return rc;
     unsigned int* status;
@@ -247,7 +252,7 @@ int dq_impl(const void* q, const void* k, const void* v, const void* do_, const 
     if (int rc = make_map_bf16(&tv, v, d, N, BHkv)) return rc;
     if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
     if (int rc = make_map_f32_out(&tdq, dq, d, N, BH)) return rc;
-    fa::DqArgs a{&tq, &tk, &tv, &tdo, &tdq, delta_ws, lse2_ws, B, Hq, N, d,
+    fa::DqArgs a{&tq, &tk, &tv, &tdo, &tdq, o, lse, delta_ws, lse2_ws, B, Hq, N, d,
                  static_cast<int>(n_pad_of(N)), Hkv, causal ? 1 : 0, scale,
                  scale * 1.4426950408889634f, status, g_timeout_ns.load()};
     return launch_rc(fa::launch_bwd_dq_bf16(a, static_cast<cudaStream_t>(stream)));
@@ -501,7 +506,18 @@ int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
 int fa_bwd_dq(const void* q, const void* k, const void* v, const void* do_,
               const float* delta_ws, const float* lse2_ws, float* dq, int B, int H, int N, int d,
               int causal, float scale, void* stream) {
-    return dq_impl(q, k, v, do_, delta_ws, lse2_ws, dq, B, H, H, N, d, causal, scale, stream);
+    // The kernel only reads the workspace on this path.
+    return dq_impl(q, k, v, nullptr, do_, nullptr, const_cast<float*>(delta_ws),
+                   const_cast<float*>(lse2_ws), dq, B, H, H, N, d, causal, scale, stream);
+}
+
+int fa_bwd_dq_preprocess(const void* q, const void* k, const void* v, const void* o,
+                         const void* do_, const float* lse, float* delta_ws, float* lse2_ws,
+                         float* dq, int B, int H, int N, int d, int causal, float scale,
+                         void* stream) {
+    if (!o || !lse) return FA_ERR_INVALID_ARG;
+    return dq_impl(q, k, v, o, do_, lse, delta_ws, lse2_ws, dq, B, H, H, N, d, causal, scale,
+                   stream);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_,
@@ -595,11 +611,11 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     }
     float* delta = static_cast<float*>(ws);
     float* lse2 = delta + static_cast<size_t>(B) * Hq * n_pad_of(N);
-    int rc = fa_bwd_preprocess(o, do_, lse, delta, lse2, B, Hq, N, d, stream);
+    // dQ with the first step fused writes D and LSE2, then dK/dV reads them.
+    int rc = dq_impl(q, k, v, o, do_, lse, delta, lse2, dq, B, Hq, Hkv, N, d, causal, scale,
+                     stream);
     if (rc == FA_OK)
         rc = dkdv_impl(q, k, v, do_, delta, lse2, dk, dv, B, Hq, Hkv, N, d, causal, scale, stream);
-    if (rc == FA_OK)
-        rc = dq_impl(q, k, v, do_, delta, lse2, dq, B, Hq, Hkv, N, d, causal, scale, stream);
     if (!workspace && cudaFreeAsync(ws, s) != cudaSuccess && rc == FA_OK) rc = FA_ERR_CUDA;
     return rc;
 }

@@ -127,8 +127,13 @@ struct DqArgs {
     const CUtensorMap* tm_v;
     const CUtensorMap* tm_do;
     const CUtensorMap* tm_dq;
-    const float* delta;
-    const float* lse2;
+    // o (bf16 [B,H,N,d]) and lse (float [B,H,N]) non-null: the kernel also
+    // does the first backward step and writes delta and lse2; null: it reads
+    // them as that step wrote them.
+    const void* o;
+    const float* lse;
+    float* delta;
+    float* lse2;
     int B, H, N, d, n_pad;  // H query heads
     int Hkv;                // K/V heads, H = n_rep * Hkv
     int causal;

@@ -84,7 +84,7 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                   16-byte aligned, or NULL: the library then allocates and
  *                   frees it on the stream (cudaMallocAsync / cudaFreeAsync).
  *
- * Runs fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq on the stream.  Every
+ * Runs fa_bwd_dq_preprocess, then fa_bwd_dkdv, on the stream.  Every
  * gradient entry is one sum in a fixed order (no atomics), so repeated calls
  * give identical bits. */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_,
@@ -104,7 +104,8 @@ int fa_bwd_preprocess(const void* o, const void* do_, const float* lse, float* d
  * Attention: Revolutionizing Transformer Efficiency", section "The Flash
  * Attention algorithm", recomputation; "FlashAttention-2", technical
  * architecture, improvement 2, parallelism over the sequence).
- * delta_ws / lse2_ws as written by fa_bwd_preprocess; dk, dv float [B,H,N,d]. */
+ * delta_ws / lse2_ws as written by fa_bwd_preprocess or fa_bwd_dq_preprocess;
+ * dk, dv float [B,H,N,d]. */
 int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
                 const float* delta_ws, const float* lse2_ws, float* dk, float* dv,
                 int B, int H, int N, int d, int causal, float scale, void* stream);
@@ -116,6 +117,20 @@ int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* do_,
 int fa_bwd_dq(const void* q, const void* k, const void* v, const void* do_,
               const float* delta_ws, const float* lse2_ws, float* dq,
               int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/* fa_bwd_dq with the first step fused into it: each dQ CTA, which already
+ * holds its dO tile in shared memory, also reads its 128 rows of O and LSE,
+ * forms D_i = sum_c dO_ic O_ic and LSE_i log2(e), uses them, and writes them
+ * to delta_ws / lse2_ws exactly as fa_bwd_preprocess would (padding rows
+ * included), ready for fa_bwd_dkdv.  The backward is then two launches: this
+ * call, then fa_bwd_dkdv.  o, lse as for fa_bwd (non-null, else
+ * FA_ERR_INVALID_ARG); other arguments as for fa_bwd_dq.  D's summation order
+ * differs from fa_bwd_preprocess's, so the two agree to FP32 rounding, not
+ * bit for bit; each is deterministic. */
+int fa_bwd_dq_preprocess(const void* q, const void* k, const void* v, const void* o,
+                         const void* do_, const float* lse, float* delta_ws, float* lse2_ws,
+                         float* dq, int B, int H, int N, int d, int causal, float scale,
+                         void* stream);
 
 /* Grouped-query attention ("FlashAttention-2", variants: multi-query and
  * grouped-query attention): Hq query heads share Hkv K/V heads, Hq = g * Hkv,

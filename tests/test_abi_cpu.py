@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
     for must in ("fa_fwd", "fa_bwd", "fa_fwd_f32", "fa_bwd_f32", "fa_bwd_workspace_bytes",
                  "fa_error_string", "fa_device_status", "fa_bwd_preprocess", "fa_bwd_dkdv",
                  "fa_bwd_dq", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fp8_quantize", "fa_fwd_fp8",
-                 "fa_last_device_status"):
+                 "fa_last_device_status", "fa_bwd_dq_preprocess"):
         assert must in names
 
 
@@ -98,6 +98,15 @@ def test_argument_checks_before_launch(fa):
     assert dq == fa.FA_ERR_INVALID_ARG
     dq = lib.fa_bwd_dq(*([0x10000] * 6 + [0x10008]), 1, 1, 16, 64, 1, 0.125, None)
     assert dq == fa.FA_ERR_MISALIGNED
+    # the fused dQ step needs O and LSE: a null one is an argument error
+    for null_at in (3, 5):
+        ptrs = [0x10000] * 9
+        ptrs[null_at] = 0
+        fused = lib.fa_bwd_dq_preprocess(*ptrs, 1, 1, 16, 64, 1, 0.125, None)
+        assert fused == fa.FA_ERR_INVALID_ARG
+    fused = lib.fa_bwd_dq_preprocess(*([0x10000] * 3 + [0x10004] + [0x10000] * 5), 1, 1, 16, 64,
+                                     1, 0.125, None)
+    assert fused == fa.FA_ERR_MISALIGNED
 
 
 def test_binding_rejects_cpu_tensors(fa):

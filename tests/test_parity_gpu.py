@@ -269,3 +269,46 @@ def test_backward_is_deterministic(fa, dev):
     torch.cuda.synchronize()
     for ga, gb in zip(a, b):
         assert torch.equal(ga, gb)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [(2, 3, 300, 128, True), (1, 2, 257, 64, False),
+                                            (1, 2, 1, 128, True), (1, 4, 1000, 64, True)])
+def test_stepwise_and_fused_backward(fa, dev, B, H, N, d, causal):
+    """The backward two ways: three launches (fa_bwd_preprocess, fa_bwd_dkdv,
+    fa_bwd_dq) and two (fa_bwd_dq_preprocess, then fa_bwd_dkdv).  Both meet
+    the oracle's gradients; the workspace each leaves holds D = rowsum(dO o O)
+    of the stored O (FP64 sum of the same BF16 values, FP32 rounding bound),
+    LSE log2(e) bit for bit alike, and 0 / +inf on padding rows."""
+    import torch
+    x = inputs(40 + N + d, B, H, N, d)
+    s = scale_for(d)
+    q, k, v, do = (to_device_bf16(x[n + "_bits"], dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, causal=causal, scale=s)
+    n_pad = (N + 127) // 128 * 128
+    ws_bytes = fa.fa_bwd_workspace_bytes(B, H, N, d)
+    got, ws = {}, {}
+    for way in ("stepwise", "fused"):
+        w = torch.full((ws_bytes // 4,), float("nan"), dtype=torch.float32, device=dev)
+        delta, lse2 = w[:B * H * n_pad].view(B * H, n_pad), w[B * H * n_pad:].view(B * H, n_pad)
+        dq, dk, dv = (torch.empty((B, H, N, d), dtype=torch.float32, device=dev) for _ in range(3))
+        if way == "stepwise":
+            fa.fa_bwd_preprocess(o, do, lse, delta, lse2)
+            fa.fa_bwd_dkdv(q, k, v, do, delta, lse2, dk, dv, causal, s)
+            fa.fa_bwd_dq(q, k, v, do, delta, lse2, dq, causal, s)
+        else:
+            fa.fa_bwd_dq_preprocess(q, k, v, o, do, lse, delta, lse2, dq, causal, s)
+            fa.fa_bwd_dkdv(q, k, v, do, delta, lse2, dk, dv, causal, s)
+        torch.cuda.synchronize()
+        got[way] = {"dq": dq, "dk": dk, "dv": dv}
+        ws[way] = (delta.cpu().numpy(), lse2.cpu().numpy())
+    refs = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], causal, s,
+                                o_storage="bf16")[:3]
+    for way in got:
+        _check_grads(got[way], refs, np.arange(B * H), B, H, N, d)
+    prod = (o.double() * do.double()).cpu().numpy().reshape(B * H, N, d)
+    d_ref, d_abs = prod.sum(axis=2), np.abs(prod).sum(axis=2)
+    for way, (delta, lse2) in ws.items():
+        err = np.abs(delta[:, :N] - d_ref)
+        assert np.all(err <= 2e-5 * d_abs + 1e-30), way
+        assert np.all(delta[:, N:] == 0.0) and np.all(np.isposinf(lse2[:, N:])), way
+    assert np.array_equal(ws["stepwise"][1], ws["fused"][1])

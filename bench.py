@@ -64,8 +64,8 @@ KERNEL_TRAFFIC = {
                  "src_sha256": "c6777adbbbc70cb68ac9a2386394915d33d1f274f201c22d612fd1bfc03b91a1"},
     "bwd_dkdv_bf16": {"bytes": 270640384 + 218950656,
                       "src_sha256": "bf2c213825688402631586a67f108ad1d2b8d8bbbd0ba2885fd9eb8c3a67a479"},
-    "bwd_dq_bf16": {"bytes": 336733184 + 112622592,
-                    "src_sha256": "1568fb97e527eaaabadbfe08648f998e2bbdac58813221b7328bd414e79656ab"},
+    "bwd_dq_bf16": {"bytes": 336697344 + 112617984,
+                    "src_sha256": "71db98e7526d7a4e05236b664aa139e3f9b57eef76d2678ac6745b8628b7dcdf"},
 }
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps

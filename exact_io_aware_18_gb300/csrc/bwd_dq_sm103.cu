@@ -87,8 +87,12 @@ struct DqBars {
     static constexpr int S_FULL = V_EMPTY + NSV;  // 2
     static constexpr int DP_FULL = S_FULL + 2;
     static constexpr int DP_EMPTY = DP_FULL + 1;
-    static constexpr int DS_FULL = DP_EMPTY + 1;
-    static constexpr int DQ_DONE = DS_FULL + 1;
+    // One dS barrier per S buffer.  S_j+2 is issued right after dQ_j, so the
+    // math warps may finish key tiles j + 1 and j + 2 before issuer A looks
+    // for dS_j+1; on a single barrier that second phase would hide the first
+    // from A's parity wait.  Per buffer, they can be at most one phase ahead.
+    static constexpr int DS_FULL = DP_EMPTY + 1;  // 2
+    static constexpr int DQ_DONE = DS_FULL + 2;
     static constexpr int DONE = DQ_DONE + 1;
     static constexpr int COUNT = DONE + 1;
 };
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(384, 1)
                        unsigned long long timeout_ns) {
     using C = DqCfg<D>;
     using Bar = DqBars<C::NSK, C::NSV>;
+    static_assert(8 * Bar::COUNT + 8 <= C::BAR_BYTES, "barrier area");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     if (smem + C::LAYOUT_BYTES > smem_raw + C::SMEM_BYTES) {
@@ -153,6 +158,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(bar(Bar::DP_FULL), 1);
         mbar_init(bar(Bar::DP_EMPTY), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::DS_FULL), C::COMPUTE_WARPS);
+        mbar_init(bar(Bar::DS_FULL + 1), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::DQ_DONE), 1);
         mbar_init(bar(Bar::DONE), 2);
         *abort_flag = 0;
@@ -237,7 +243,7 @@ __global__ void __launch_bounds__(384, 1)
             if (ok && n_kv > 1) ok = issue_s(1);
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int st = j % C::NSK;
-                ok = mbar_wait(bar(Bar::DS_FULL), j & 1, wc);
+                ok = mbar_wait(bar(Bar::DS_FULL + (j & 1)), (j >> 1) & 1, wc);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t s_cols = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
@@ -399,7 +405,7 @@ __global__ void __launch_bounds__(384, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(Bar::DS_FULL));
+            if (lane == 0) mbar_arrive(bar(Bar::DS_FULL + (j & 1)));
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DQ_DONE), 0, wc));
         if (ok) {

@@ -247,6 +247,14 @@ def measure_next_rows(fa, torch, q, k, v, do, stream, iters=20):
                                                            stream), iters)
     bwd_ms = _timed(torch, stream, lambda: fa.fa_bwd_gqa(q, kg, vg, o, do, lse, dq, dk, dv,
                                                            CAUSAL, scale, ws, stream), iters)
+    # The backward's first step as a launch of its own (the step-wise calls; the
+    # timed step fuses it into dQ): HBM-bound, O and dO read, D and LSE2 written.
+    n_pad = (N + 127) // 128 * 128
+    delta = ws[:B * H * n_pad].view(B * H, n_pad)
+    lse2 = ws[B * H * n_pad:].view(B * H, n_pad)
+    pre_ms = _timed(torch, stream, lambda: fa.fa_bwd_preprocess(o, do, lse, delta, lse2, stream),
+                    iters)
+    pre_bytes = 2 * B * H * N * D * 2 + B * H * N * 4 + 2 * B * H * n_pad * 4
     # Split-KV decode: one new query per head against a long cache, grouped
     # K/V heads.  HBM-bound (K and V are read once); seeded synthetic inputs.
     db, dhq, dhkv, dnq, dnk = 4, 32, 8, 1, 16384
@@ -329,6 +337,14 @@ def measure_next_rows(fa, torch, q, k, v, do, stream, iters=20):
             "gbs": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1),
             "frac_of_hbm": round(dec_bytes / (dec_ms * 1e-3) / 1e9 / hbm, 4),
             "tflops": round(dec_flops / (dec_ms * 1e-3) / 1e12, 2)},
+        "bwd_preprocess_standalone": {
+            "workload": f"B={B} H={H} N={N} d={D}: D = rowsum(dO o O) and LSE log2(e) as a launch "
+                        "of its own (the timed step fuses it into dQ)",
+            "ms": round(pre_ms, 4),
+            "bound": "hbm",
+            "algorithmic_bytes": pre_bytes,
+            "gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(pre_bytes / (pre_ms * 1e-3) / 1e9 / hbm, 4)},
         "gqa": {"workload": f"B={B} Hq={H} Hkv={hkv} N={N} d={D} causal, bf16",
                 "fwd_ms": round(fwd_ms, 4),
                 "fwd_tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),

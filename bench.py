@@ -60,12 +60,12 @@ def kernel_src_sha256(name: str) -> str:
 
 KERNEL_TRAFFIC = {
     # profiles/kernels_training_step_b8_h16_n2048_d128_causal.md (ncu --set full)
-    "fwd_bf16": {"bytes": 201417984 + 48139776,
-                 "src_sha256": "c6777adbbbc70cb68ac9a2386394915d33d1f274f201c22d612fd1bfc03b91a1"},
-    "bwd_dkdv_bf16": {"bytes": 270640384 + 218950656,
-                      "src_sha256": "bf2c213825688402631586a67f108ad1d2b8d8bbbd0ba2885fd9eb8c3a67a479"},
-    "bwd_dq_bf16": {"bytes": 336697344 + 112617984,
-                    "src_sha256": "71db98e7526d7a4e05236b664aa139e3f9b57eef76d2678ac6745b8628b7dcdf"},
+    "fwd_bf16": {"bytes": 201437696 + 48240640,
+                "src_sha256": "a139f314cd8d4ab45530e24a33c32cc48cbad0241d8d214647d93dd4294b316d"},
+    "bwd_dkdv_bf16": {"bytes": 270639616 + 219129856,
+                     "src_sha256": "dca583ce6a2c38bd31a4694397f3a0981db558d899f19ad09f06b8f831174f36"},
+    "bwd_dq_bf16": {"bytes": 336706560 + 112510976,
+                   "src_sha256": "b674dc93a94af3ee3b680b85db46f53854e8e100b6ee4d9d3475f44c9a9b63a7"},
 }
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps

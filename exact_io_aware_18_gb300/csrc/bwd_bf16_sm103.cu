@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const WaitCtx wc{status, timeout_ns, abort_flag};
+    pdl_wait_then_release();
 
     // Item k of this CTA from the queue (single-thread roles); -1 at the end
     // of the work or when a wait gave up.
@@ -550,11 +551,11 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     if (group < 1) group = 1;
     const long long n_items = static_cast<long long>(a.B) * a.Hkv * n_tiles;
     const int grid = static_cast<int>(n_items < a.num_sms ? n_items : a.num_sms);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dk, *a.tm_dv, a.delta, a.lse2, a.N, a.n_pad,
-        a.B * a.Hkv, a.Hkv, a.H / a.Hkv, n_tiles, group, a.scale, a.scale_log2, a.status,
-        a.timeout_ns, a.work);
-    return cudaGetLastError();
+    e = launch_overlapped(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tm_q,
+                          *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dk, *a.tm_dv, a.delta, a.lse2, a.N,
+                          a.n_pad, a.B * a.Hkv, a.Hkv, a.H / a.Hkv, n_tiles, group, a.scale,
+                          a.scale_log2, a.status, a.timeout_ns, a.work);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

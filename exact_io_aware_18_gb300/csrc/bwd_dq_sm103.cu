@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const WaitCtx wc{status, timeout_ns, abort_flag};
+    pdl_wait_then_release();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producers
@@ -460,11 +461,11 @@ cudaError_t launch_t(const DqArgs& a, cudaStream_t stream) {
     int group = 128 / n_tiles;
     if (group < 1) group = 1;
     dim3 grid(n_tiles, a.H, a.B);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, static_cast<const uint4*>(a.o), a.lse,
-        a.delta, a.lse2, a.N, a.n_pad, a.B * a.H,
-        a.H, a.H / a.Hkv, n_tiles, group, a.scale, a.scale_log2, a.status, a.timeout_ns);
-    return cudaGetLastError();
+    e = launch_overlapped(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tm_q, *a.tm_k,
+                          *a.tm_v, *a.tm_do, *a.tm_dq, static_cast<const uint4*>(a.o), a.lse,
+                          a.delta, a.lse2, a.N, a.n_pad, a.B * a.H, a.H, a.H / a.Hkv, n_tiles,
+                          group, a.scale, a.scale_log2, a.status, a.timeout_ns);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

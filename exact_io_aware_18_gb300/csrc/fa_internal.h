@@ -6,8 +6,30 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <utility>
 
 namespace fa {
+
+// Launches kern with programmatic stream serialization: its CTAs may be
+// scheduled while the kernel before it in the stream finishes (on the SMs
+// that kernel's CTAs leave).  The kernel itself waits for its predecessor
+// (pdl_wait_then_release, sm103_primitives.cuh) before it touches global
+// memory, so only its launch and set-up overlap.
+template <typename... Params, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Forward (BF16).  Tensor maps view Q, K, V, O as 3-D arrays
 // (d, N, B*H) of bf16 with 128 x 64 boxes and 128-byte swizzle.

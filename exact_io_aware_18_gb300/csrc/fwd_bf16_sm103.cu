@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const WaitCtx wc{status, timeout_ns, abort_flag};
+    pdl_wait_then_release();
 
     // Tile k of this CTA from the queue (single-thread roles).  Returns -1 at
     // the end of the work or when a wait gave up.
@@ -696,11 +697,12 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     if (group < 1) group = 1;
     const long long n_items = static_cast<long long>(a.B) * a.H * n_tiles * a.n_splits;
     const int grid = static_cast<int>(n_items < a.num_sms ? n_items : a.num_sms);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse, a.N, a.B * a.H, a.H, a.H / a.Hkv, n_tiles,
-        group, a.scale_log2, a.status, a.timeout_ns, a.work, a.Nk, a.n_splits, a.chunk_tiles,
-        a.o_part, a.lse_part, a.q_scale, a.k_scale);
-    return cudaGetLastError();
+    e = launch_overlapped(
+        kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tm_q, *a.tm_k, *a.tm_v,
+        *a.tm_o, a.lse, a.N, a.B * a.H, a.H, a.H / a.Hkv, n_tiles, group, a.scale_log2, a.status,
+        a.timeout_ns, a.work, a.Nk, a.n_splits, a.chunk_tiles, a.o_part, a.lse_part, a.q_scale,
+        a.k_scale);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

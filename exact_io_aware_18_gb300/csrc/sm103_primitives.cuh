@@ -159,6 +159,19 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Programmatic dependent launch.  Waits until the kernel launched before this
+// one in the stream has completed and its writes are visible (at once when
+// this launch did not ask to overlap it), then lets the next kernel's CTAs be
+// scheduled: they start on SMs that this kernel's CTAs leave, do their own
+// set-up and wait here in turn.  Called by every thread after the CTA's
+// set-up and before its first access to global memory, so no read or write
+// can overtake the previous kernel's, and at most two kernels of a stream are
+// ever resident at once.
+__device__ __forceinline__ void pdl_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -312,3 +312,42 @@ def test_stepwise_and_fused_backward(fa, dev, B, H, N, d, causal):
         assert np.all(err <= 2e-5 * d_abs + 1e-30), way
         assert np.all(delta[:, N:] == 0.0) and np.all(np.isposinf(lse2[:, N:])), way
     assert np.array_equal(ws["stepwise"][1], ws["fused"][1])
+
+
+def test_back_to_back_calls_match_synchronised_calls(fa, dev):
+    """The forward, dQ and dK/dV kernels are launched so that each one's set-up
+    overlaps the end of the kernel before it; each still waits for that kernel
+    before it touches memory.  Calls queued back to back on shared O, LSE and
+    workspace buffers (the next forward overwrites the O the last dQ read; the
+    next dQ overwrites the D / LSE2 the last dK/dV read) give the same bits as
+    the same calls separated by device synchronisations."""
+    import torch
+    B, H, N, d = 2, 4, 1000, 128
+    s = scale_for(d)
+    ins = []
+    for i in range(3):
+        x = inputs(60 + i, B, H, N, d)
+        ins.append(tuple(to_device_bf16(x[n + "_bits"], dev) for n in ("q", "k", "v", "do")))
+    o = torch.empty(B, H, N, d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d) // 4, dtype=torch.float32, device=dev)
+
+    def run(sync):
+        grads = [tuple(torch.empty(B, H, N, d, dtype=torch.float32, device=dev) for _ in range(3))
+                 for _ in ins]
+        for (q, k, v, do), (dq, dk, dv) in zip(ins, grads):
+            fa.fa_fwd(q, k, v, o, lse, True, s)
+            if sync:
+                torch.cuda.synchronize()
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, True, s, ws)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return grads, o.clone(), lse.clone()
+
+    queued, o_q, lse_q = run(False)
+    synced, o_s, lse_s = run(True)
+    assert torch.equal(o_q, o_s) and torch.equal(lse_q, lse_s)
+    for gq, gs in zip(queued, synced):
+        for a, b in zip(gq, gs):
+            assert torch.equal(a, b)

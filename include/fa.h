@@ -26,6 +26,12 @@
  *     pointer must be 16-byte aligned.
  *   - stream is a cudaStream_t passed as void* (NULL: the legacy default
  *     stream).  Work is enqueued on it and the call returns without waiting.
+ *     The tensor-core forward and backward kernels are launched with
+ *     programmatic stream serialization: their CTAs may be scheduled and set
+ *     up while the kernel before them in the stream finishes, but each waits
+ *     for that kernel to complete before it reads or writes any global
+ *     memory, so the stream's ordering is the same as for plain launches
+ *     (also inside a captured CUDA graph).
  *   - Return value: FA_OK, or a negative fa_status.  Argument errors
  *     (INVALID_ARG, UNSUPPORTED, MISALIGNED) are found before anything is
  *     launched.  FA_ERR_CUDA reports a launch error.  A kernel that gives up

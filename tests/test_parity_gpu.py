@@ -351,3 +351,38 @@ def test_back_to_back_calls_match_synchronised_calls(fa, dev):
     for gq, gs in zip(queued, synced):
         for a, b in zip(gq, gs):
             assert torch.equal(a, b)
+
+
+def test_cuda_graph_capture_replays_the_step(fa, dev):
+    """Forward and backward captured into one CUDA graph (the overlapped
+    launches become programmatic edges of the graph) replay to the bits of
+    the same calls made eagerly."""
+    import torch
+    B, H, N, d = 1, 4, 700, 128
+    s = scale_for(d)
+    x = inputs(70, B, H, N, d)
+    q, k, v, do = (to_device_bf16(x[n + "_bits"], dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty(B, H, N, d, dtype=torch.float32, device=dev) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d) // 4, dtype=torch.float32, device=dev)
+    outs = (o, lse, dq, dk, dv)
+
+    def step():
+        fa.fa_fwd(q, k, v, o, lse, True, s)
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, True, s, ws)
+
+    step()
+    torch.cuda.synchronize()
+    want = [t.clone() for t in outs]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        for t in outs:
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for got, ref in zip(outs, want):
+            assert torch.equal(got, ref)
+    assert fa.fa_device_status(clear=True) == fa.FA_OK

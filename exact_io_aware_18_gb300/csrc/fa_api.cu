@@ -201,7 +201,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (int rc = work_slot(&work, &sms)) return rc;
     fa::FwdArgs a{&tq, &tk, &tv, &to, lse, B, Hq, N, d, Hkv, causal ? 1 : 0,
                   scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms,
-                  /*Nk=*/N, /*n_splits=*/1, /*chunk_tiles=*/0, nullptr, nullptr};
+                  /*Nk=*/N, /*n_splits=*/1, /*chunk_tiles=*/0, nullptr, nullptr,
+                  /*q_scale=*/nullptr, /*k_scale=*/nullptr};
     return launch_rc(fa::launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -412,7 +413,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
         // The split kernel stores no O tile: the Q map stands in for O's.
         fa::FwdArgs a{&tq, &tk, &tv, &tq, nullptr, B, Hkv, rows, d, Hkv, 0,
                       scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms,
-                      Nk, plan.n_splits, plan.chunk_tiles, o_part, lse_part};
+                      Nk, plan.n_splits, plan.chunk_tiles, o_part, lse_part,
+                      /*q_scale=*/nullptr, /*k_scale=*/nullptr};
         rc = launch_rc(fa::launch_fwd_splitkv_bf16(a, st));
         if (rc == FA_OK) {
             // Partials and outputs share the row order [B, Hkv, g, Nq] = [B, Hq, Nq].

@@ -47,6 +47,7 @@ struct QuantCfg {
     static constexpr int BOX_BYTES = 128 * 128;   // one 128-row x 128-byte box
     static constexpr int IN_BYTES = KB * BOX_BYTES;
     static constexpr int OUT_BYTES = 128 * D;     // one tile of codes, over its input
+    static_assert(OUT_BYTES <= IN_BYTES, "the codes are written over their tile's input");
     static constexpr int NBUF = 2;
     static constexpr int OFF_IN = 0;
     static constexpr int OFF_BAR = OFF_IN + NBUF * IN_BYTES;

@@ -39,10 +39,11 @@ METRIC = ("attention fwd/bwd TFLOP/s (4BHN²d, causal halved) and % of GB300 BF1
 B, H, N, D, CAUSAL, SEED = 8, 16, 2048, 128, True, 4
 WORKLOAD = "training step fwd+bwd, bf16, B=8 H=16 N=2048 d=128, causal, scale=1/sqrt(d), seed 4"
 
-# DRAM traffic of one launch of a kernel at this workload, from the ncu
-# summaries under profiles/; valid only for the kernel source it was measured
-# on (sha256 of its .cu file followed by the shared primitives header), else
-# the roofline reports traffic as null.
+# DRAM traffic of one launch of a kernel at this workload, read from an ncu
+# capture of that kernel (dram__bytes_read.sum + dram__bytes_write.sum); valid
+# only for the kernel source it was measured on (sha256 of its .cu file
+# followed by the shared primitives header), else the roofline reports
+# traffic as null.
 CSRC = os.path.join(ROOT, "exact_io_aware_18_gb300", "csrc")
 KERNEL_SRC = {"fwd_bf16": os.path.join(CSRC, "fwd_bf16_sm103.cu"),
               "bwd_dkdv_bf16": os.path.join(CSRC, "bwd_bf16_sm103.cu"),
@@ -59,7 +60,6 @@ def kernel_src_sha256(name: str) -> str:
 
 
 KERNEL_TRAFFIC = {
-    # profiles/kernels_training_step_b8_h16_n2048_d128_causal.md (ncu --set full)
     "fwd_bf16": {"bytes": 201437696 + 48240640,
                 "src_sha256": "a139f314cd8d4ab45530e24a33c32cc48cbad0241d8d214647d93dd4294b316d"},
     "bwd_dkdv_bf16": {"bytes": 270639616 + 219129856,
@@ -70,6 +70,9 @@ KERNEL_TRAFFIC = {
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Datasheet dense BF16 tensor rate of one GPU: NVIDIA quotes 36 PFLOP/s BF16
+# for an 8-GPU HGX B300 board with 2:4 sparsity, i.e. 2.25 PFLOP/s dense per GPU.
+NOMINAL_BF16_TFLOPS = 2250.0
 
 
 def dist_env():
@@ -177,6 +180,77 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(s[1] for s in used),
                 "sm_max_mhz": max(s[2] for s in used), "reasons": reasons,
                 "samples": len(used), "samples_inside_timed_region": len(inside)}
+
+
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML every millisecond,
+    so that even a timed region of a few milliseconds holds several samples.
+    Reads only; falls back to nothing when NVML cannot be loaded."""
+
+    # nvmlClocksEventReasons bits -> the names nvidia-smi uses
+    BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch, device, period_s: float = 0.001):
+        self.samples = []  # (t, sm, max, reasons)
+        self.period_s = period_s
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.nvml = None
+        self.handle = None
+        try:
+            import ctypes
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(device)
+            bus = None
+            if all(hasattr(props, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+                bus = (f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:"
+                       f"{props.pci_device_id:02X}.0").encode()
+            if bus is None or nvml.nvmlDeviceGetHandleByPciBusId_v2(
+                    ctypes.c_char_p(bus), ctypes.byref(handle)) != 0:
+                return
+            self.nvml, self.handle, self.ctypes = nvml, handle, ctypes
+        except (OSError, AttributeError):
+            self.nvml = None
+
+    def _read(self):
+        c = self.ctypes
+        sm, mx, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        get_reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_flag.is_set():
+            ok = (self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, c.byref(sm)) == 0 and
+                  self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, c.byref(mx)) == 0 and
+                  get_reasons(self.handle, c.byref(rs)) == 0)
+            if ok:
+                reasons = [n for b, n in self.BITS.items() if rs.value & b]
+                self.samples.append((time.monotonic(), float(sm.value), float(mx.value), reasons))
+            time.sleep(self.period_s)
+
+    def start(self):
+        if self.nvml is None:
+            return False
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return True
+
+    def stop(self):
+        self.stop_flag.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return None
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": sorted({r for s in inside for r in s[3]}),
+                "samples": len(inside), "samples_inside_timed_region": len(inside),
+                "source": "NVML, 1 ms period"}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -354,6 +428,98 @@ def measure_next_rows(fa, torch, q, k, v, do, stream, iters=20):
     }
 
 
+def frac(tflops, peak):
+    return round(tflops / peak, 4)
+
+
+def time_training_step(fa, torch, stream, t, causal, steps, warmup):
+    """Mean CUDA-event time of each kernel of the step (forward, dQ with the
+    first backward step fused, dK/dV) over `steps` back-to-back steps after
+    `warmup` untimed ones; t holds the step's device tensors."""
+    q, k, v, do, o, lse, dq, dk, dv, delta, lse2 = t
+    d = q.shape[-1]
+    scale = fa.default_scale(d)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, causal, scale, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_bwd_dq_preprocess(q, k, v, o, do, lse, delta, lse2, dq, causal, scale, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        fa.fa_bwd_dkdv(q, k, v, do, delta, lse2, dk, dv, causal, scale, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        step(events[i])
+    torch.cuda.synchronize()
+    return tuple(statistics.mean(e[a].elapsed_time(e[a + 1]) for e in events) for a in range(3))
+
+
+def measure_training_rows(fa, torch, dev, stream, steps, warmup):
+    """Forward + backward at B=4 H=16 N=4096 d=128 (the shape of the N = 4096
+    workload, seed 2, with dO drawn after Q, K, V), causal and not: the
+    sequence length where the tensor-core targets are set.  Timed like the
+    headline step; each kernel against the measured burst peak and the
+    datasheet figure."""
+    import fa_inputs
+    b, h, n, d = 4, 16, 4096, 128
+    x = fa_inputs.attention_inputs(2, b, h, n, d, "bf16")
+
+    def put(name):
+        return torch.from_numpy(x[name + "_bits"].view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v, do = (put(nm) for nm in ("q", "k", "v", "do"))
+    del x
+    o = torch.empty_like(q)
+    lse = torch.empty((b, h, n), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty((b, h, n, d), dtype=torch.float32, device=dev) for _ in range(3))
+    n_pad = (n + 127) // 128 * 128
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(b, h, n, d) // 4, dtype=torch.float32, device=dev)
+    delta = ws[:b * h * n_pad].view(b * h, n_pad)
+    lse2 = ws[b * h * n_pad:].view(b * h, n_pad)
+    peaks, kind = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    rows = {}
+    for causal in (True, False):
+        f_fwd, f_bwd = step_flops(b, h, n, d, causal)
+        fwd_ms, dq_ms, dkdv_ms = time_training_step(
+            fa, torch, stream, (q, k, v, do, o, lse, dq, dk, dv, delta, lse2), causal,
+            steps, warmup)
+        bwd_ms = dq_ms + dkdv_ms
+        tf = {"fwd": f_fwd / (fwd_ms * 1e-3) / 1e12,
+              "bwd_dq": 1.5 * f_fwd / (dq_ms * 1e-3) / 1e12,
+              "bwd_dkdv": 2.0 * f_fwd / (dkdv_ms * 1e-3) / 1e12,
+              "bwd": f_bwd / (bwd_ms * 1e-3) / 1e12}
+        rows["causal" if causal else "non_causal"] = {
+            "fwd_ms": round(fwd_ms, 4), "bwd_dq_ms": round(dq_ms, 4),
+            "bwd_dkdv_ms": round(dkdv_ms, 4), "bwd_ms": round(bwd_ms, 4),
+            "fwd_tflops": round(tf["fwd"], 2),
+            "fwd_frac_of_burst": frac(tf["fwd"], burst),
+            "fwd_frac_of_nominal": frac(tf["fwd"], NOMINAL_BF16_TFLOPS),
+            "bwd_tflops": round(tf["bwd"], 2),
+            "bwd_frac_of_burst": frac(tf["bwd"], burst),
+            "bwd_frac_of_nominal": frac(tf["bwd"], NOMINAL_BF16_TFLOPS),
+            "bwd_dq_own_tflops": round(tf["bwd_dq"], 2),
+            "bwd_dkdv_own_tflops": round(tf["bwd_dkdv"], 2),
+        }
+    if fa.fa_device_status(clear=True) != fa.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait in the N = 4096 training rows")
+    return dict(rows, workload="fwd+bwd, bf16, B=4 H=16 N=4096 d=128, seed 2 (Q, K, V, dO)",
+                steps=steps, warmup=warmup,
+                flops="forward 4 B H N^2 d, backward 2.5x that, causal halved; each kernel's "
+                      "own products: dQ 1.5x, dK/dV 2x the forward",
+                peaks=f"burst bf16_tflops ({kind}) {burst}; datasheet dense BF16 "
+                      f"{NOMINAL_BF16_TFLOPS}")
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -417,6 +583,8 @@ def run_gpu(args):
             pass
     sampler = ClockSampler(gpu_index)
     sampler.start()
+    fine = NvmlClockSampler(torch, dev)
+    fine.start()
     time.sleep(0.3)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
@@ -498,7 +666,12 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(torch, e0.elapsed_time(e1) / e2e_steps, dev, world)
     sampler.stop()
-    next_rows = measure_next_rows(fa, torch, q, k, v, do, stream) if rank == 0 else None
+    fine.stop()
+    next_rows = None
+    if rank == 0:
+        next_rows = measure_next_rows(fa, torch, q, k, v, do, stream)
+        next_rows["training_step_n4096"] = measure_training_rows(
+            fa, torch, dev, stream, max(1, min(args.steps, 200)), args.warmup)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
 
@@ -511,7 +684,10 @@ def run_gpu(args):
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_tflops(world, f_fwd + f_bwd, ms_per_step)
     peaks, peak_kind = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    # The timed region is a few milliseconds to a second of kernels: the
+    # burst figure (a GEMM timed alone) is the denominator, not the rate a
+    # GEMM settles at after seconds under the power cap.
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     # Each kernel's own GEMM FLOPs per launch: the forward does 2 GEMMs per
     # (Q tile, key tile) pair, dK/dV 4 (S^T, dP^T, dV, dK), dQ 3 (S, dP, dQ;
     # S and dP recomputed).  The step metric counts 2.5x the forward for the
@@ -528,7 +704,8 @@ def run_gpu(args):
             traffic = rec["bytes"]
     except (OSError, KeyError):
         pass
-    clocks = sampler.summary(t_wall0, t_wall1)
+    clocks = fine.summary(t_wall0, t_wall1) or sampler.summary(t_wall0, t_wall1)
+    mhz = clocks.get("sm_mhz") or None
 
     # CPU baseline: the oracle as it stands on a bounded sample (whole heads).
     cores = oracle_cores()
@@ -551,8 +728,13 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "causal": CAUSAL,
                    "l2": "inputs larger than L2: Q, K, V, dO are 4 x 64 MiB per step"},
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
-                     "peak": peak, "peak_kind": f"bf16_tflops_sustained ({peak_kind})",
-                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic},
+                     "peak": peak, "peak_kind": f"bf16_tflops, burst ({peak_kind})",
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "frac_of_nominal": frac(achieved, NOMINAL_BF16_TFLOPS),
+                     "nominal_peak": NOMINAL_BF16_TFLOPS,
+                     "flops_counted": "the kernel's own products per launch (dK/dV: S^T, dP^T, "
+                                      "dV, dK = 2x the forward; dQ: S, dP, dQ = 1.5x)",
+                     "traffic": traffic},
         "cpu_baseline": {"value": round(cpu_flops / cpu_s / 1e12, 6), "unit": "TFLOP/s",
                          "cores": cores, "kind": "oracle",
                          "sample": f"{n_heads} of {B * H} heads (whole heads, fwd+bwd), "
@@ -564,21 +746,40 @@ def run_gpu(args):
                           "while step i computes (two device buffer sets)"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
-        "kernels": {
-            "fwd": {"ms": round(fwd_ms, 4), "tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2),
-                    "frac_of_peak": round(f_fwd / (fwd_ms * 1e-3) / 1e12 / peak, 4)},
-            "bwd_dq": {"ms": round(dq_ms, 4),
-                       "tflops": round(kern_flops["bwd_dq_bf16"] / (dq_ms * 1e-3) / 1e12, 2),
-                       "includes": "the first backward step: D = rowsum(dO o O), LSE log2(e)"},
-            "bwd_dkdv": {"ms": round(dkdv_ms, 4),
-                         "tflops": round(kern_flops["bwd_dkdv_bf16"] / (dkdv_ms * 1e-3) / 1e12, 2)},
-            "bwd_total_tflops": round(f_bwd / ((dkdv_ms + dq_ms) * 1e-3) / 1e12, 2),
-        },
+        "kernels": kernel_table(fwd_ms, dq_ms, dkdv_ms, f_fwd, f_bwd, value, peak, mhz),
         "next_rows": next_rows,
     }
     print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def kernel_table(fwd_ms, dq_ms, dkdv_ms, f_fwd, f_bwd, step_tflops, burst, mhz):
+    """Each kernel's time and rate, as fractions of the measured burst peak
+    and of the datasheet figure, with time x median SM clock beside them.
+    The metric's own rates: forward 4 B H N^2 d, backward 2.5x (causal
+    halved); a kernel's own rate counts the products it executes."""
+    def row(ms, flops, **extra):
+        tf = flops / (ms * 1e-3) / 1e12
+        r = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac_of_burst": frac(tf, burst),
+             "frac_of_nominal": frac(tf, NOMINAL_BF16_TFLOPS)}
+        if mhz:
+            r["kcycles_at_median_sm_clock"] = round(ms * mhz, 1)
+        r.update(extra)
+        return r
+
+    bwd_ms = dq_ms + dkdv_ms
+    return {
+        "fwd": row(fwd_ms, f_fwd),
+        "bwd_dq": row(dq_ms, 1.5 * f_fwd, flops="own products S, dP, dQ (1.5x the forward)",
+                      includes="the first backward step: D = rowsum(dO o O), LSE log2(e)"),
+        "bwd_dkdv": row(dkdv_ms, 2.0 * f_fwd, flops="own products S^T, dP^T, dV, dK (2x)"),
+        "bwd": row(bwd_ms, f_bwd, flops="the metric's 2.5x the forward"),
+        "bwd_total_tflops": round(f_bwd / (bwd_ms * 1e-3) / 1e12, 2),
+        "step": {"tflops": round(step_tflops, 2), "frac_of_burst": frac(step_tflops, burst),
+                 "frac_of_nominal": frac(step_tflops, NOMINAL_BF16_TFLOPS)},
+        "peaks": {"burst_measured": burst, "nominal_dense_bf16": NOMINAL_BF16_TFLOPS},
+    }
 
 
 # ---------------------------------------------------------------- reference arm

@@ -21,13 +21,13 @@
 // later (padding rows included), so nothing needs clearing between calls;
 // but two calls that run on the GPU at the same time (on different streams,
 // say) would race on the array.
-#include <cmath>
 #include <cstdint>
 #include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "../../include/fa.h"
+#include "fa_internal.h"
 
 namespace {
 
@@ -58,14 +58,10 @@ int scratch_ptr(float** out) {
 extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                               const void* do_, const float* lse, float* dq, float* dk, float* dv,
                               int B, int H, int N, int d, int causal, float scale, void* stream) {
-    const void* ptrs[] = {q, k, v, o, do_, lse, dq, dk, dv};
-    for (const void* p : ptrs)
-        if (!p) return FA_ERR_INVALID_ARG;
-    for (const void* p : ptrs)
-        if (reinterpret_cast<uintptr_t>(p) & 15u) return FA_ERR_MISALIGNED;
-    if (B < 1 || H < 1 || N < 1 || !(scale > 0.f) || !std::isfinite(scale))
-        return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    // fa_bwd's own checks first, so both entry points give the same status for
+    // the same arguments; only then the size of the built-in scratch.
+    if (int rc = fa::check_bwd_args(q, k, v, o, do_, lse, dq, dk, dv, B, H, N, d, scale))
+        return rc;
     const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
     if (need == 0) return FA_ERR_INVALID_ARG;
     if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_NO_MEMORY;

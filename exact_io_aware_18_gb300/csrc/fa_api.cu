@@ -599,8 +599,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
              const float* lse, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int N,
              int d, int causal, float scale, void* workspace, size_t workspace_bytes,
              void* stream) {
-    if (int rc = check_ptrs({q, k, v, o, do_, lse, dq, dk, dv})) return rc;
-    if (int rc = check_shape(B, Hq, N, d, scale)) return rc;
+    if (int rc = fa::check_bwd_args(q, k, v, o, do_, lse, dq, dk, dv, B, Hq, N, d, scale))
+        return rc;
     if (int rc = check_heads(Hq, Hkv)) return rc;
     const size_t need = fa_bwd_workspace_bytes(B, Hq, N, d);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -623,3 +623,14 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
 }
 
 }  // namespace
+
+namespace fa {
+
+int check_bwd_args(const void* q, const void* k, const void* v, const void* o, const void* do_,
+                   const float* lse, const float* dq, const float* dk, const float* dv, int B,
+                   int H, int N, int d, float scale) {
+    if (int rc = check_ptrs({q, k, v, o, do_, lse, dq, dk, dv})) return rc;
+    return check_shape(B, H, N, d, scale);
+}
+
+}  // namespace fa

@@ -189,6 +189,13 @@ struct F32Args {
 cudaError_t launch_fwd_f32(const F32Args& a, cudaStream_t stream);
 cudaError_t launch_bwd_f32(const F32Args& a, cudaStream_t stream);
 
+// The argument checks fa_bwd makes before it looks at its workspace (null
+// and misaligned pointers, sizes, head dimension, scale), in the same order
+// and with the same status codes; fa_bwd_noalloc runs them first too.
+int check_bwd_args(const void* q, const void* k, const void* v, const void* o, const void* do_,
+                   const float* lse, const float* dq, const float* dk, const float* dv, int B,
+                   int H, int N, int d, float scale);
+
 // Failure-detection self-test kernel (waits on a barrier nobody arrives at).
 cudaError_t launch_wait_timeout_selftest(unsigned int* status, unsigned long long timeout_ns,
                                          cudaStream_t stream);

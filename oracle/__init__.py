@@ -54,10 +54,11 @@ def _load():
         lib.oracle_probs.argtypes = [_dp, _dp, _i64, _i64, ctypes.c_int, ctypes.c_double, _dp]
         lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64, ctypes.c_int,
                                    ctypes.c_double, ctypes.c_int, _ip, _i64, _dp, _dp, _dp, _dp]
+        lib.oracle_round_bf16_array.argtypes = [_dp, _i64, _dp]
         lib.oracle_round_bf16.argtypes = [ctypes.c_double]
         lib.oracle_round_bf16.restype = ctypes.c_double
         for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_probs, lib.oracle_bwd,
-                  lib.oracle_num_threads):
+                  lib.oracle_num_threads, lib.oracle_round_bf16_array):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -134,6 +135,24 @@ _O_STORAGE = {"exact": 0, "bf16": 1, "f32": 2}
 def round_bf16(x: float) -> float:
     """x rounded to the nearest bfloat16 value, ties to even (normal range)."""
     return float(_load().oracle_round_bf16(float(x)))
+
+
+def stored_output(o, o_storage: str = "bf16") -> np.ndarray:
+    """O as a backward is handed it when the forward stores it in o_storage:
+    "bf16" (each value rounded as round_bf16 rounds it), "f32" or "exact".
+    attention_bwd forms D from exactly these values, so a backward given
+    them as its O input is compared with attention_bwd on equal inputs."""
+    if o_storage not in _O_STORAGE:
+        raise ValueError(f"o_storage must be one of {sorted(_O_STORAGE)}")
+    o = _f64(o)
+    if o_storage == "exact":
+        return o.copy()
+    if o_storage == "f32":
+        return o.astype(np.float32).astype(np.float64)
+    out = np.empty_like(o)
+    _check(_load().oracle_round_bf16_array(_ptr(o), o.size, _ptr(out)),
+           "oracle_round_bf16_array")
+    return out
 
 
 def attention_bwd(q, k, v, do, causal: bool, scale: float, heads=None, o_storage="exact"):

@@ -185,6 +185,13 @@ double oracle_round_bf16(double x) {
     return ldexp(r, e - 8);
 }
 
+/* x[i] rounded as oracle_round_bf16 rounds it, for i < n. */
+int oracle_round_bf16_array(const double* x, int64_t n, double* out) {
+    if (n < 0 || (n > 0 && (!x || !out))) return -1;
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_round_bf16(x[i]);
+    return 0;
+}
+
 static double stored_output(double x, int o_storage) {
     if (o_storage == 1) return oracle_round_bf16(x);
     if (o_storage == 2) return (double)(float)x;

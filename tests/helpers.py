@@ -1,6 +1,8 @@
 """Shared test utilities: input upload, error metrics, row sampling."""
 
+import json
 import math
+import os
 
 import numpy as np
 
@@ -61,3 +63,29 @@ def sample_rows(seed, BH, N, n_random, heads=None):
 
 def inputs(seed, B, H, N, d, dtype="bf16", names=("q", "k", "v", "do")):
     return fa_inputs.attention_inputs(seed, B, H, N, d, dtype, names)
+
+
+def oracle_o_lse_on_device(x, causal, scale, device):
+    """The oracle's O rounded to bf16 (as the oracle rounds the O its
+    backward forms D from) and its LSE rounded to float32, on the device:
+    the inputs a backward gets when compared with the oracle on equal inputs."""
+    import torch
+    import oracle
+    ro, rl = oracle.attention_fwd(x["q"], x["k"], x["v"], causal, scale)
+    ob = oracle.stored_output(ro, "bf16").astype(np.float32)
+    bits = fa_inputs.bf16_bits(ob)  # exact: ob already holds bf16 values
+    o = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    lse = torch.from_numpy(np.ascontiguousarray(rl, dtype=np.float32))
+    return o.to(device), lse.to(device)
+
+
+def diagnostic(what, **values):
+    """A measured figure that is reported, not asserted: printed (visible
+    with pytest -s or -rP) and, when FA_DIAGNOSTICS names a file, appended
+    to it as one JSON line."""
+    line = {"what": what, **{k: float(v) for k, v in values.items()}}
+    print("DIAGNOSTIC", json.dumps(line))
+    path = os.environ.get("FA_DIAGNOSTICS")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(line) + "\n")

@@ -7,6 +7,7 @@ scale) would break.  All run on the CPU in well under a minute.
 """
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -317,6 +318,31 @@ def test_round_bf16_matches_float32_bit_rounding(oracle_lib):
     assert np.array_equal(got, want)
 
 
+def test_stored_output_rounds_like_the_generator(oracle_lib):
+    # stored_output is the O a backward is handed: each value rounded by the
+    # oracle's own bf16 rounding, which agrees with the input generator's
+    # independent bit arithmetic on float32 values (one rounding either way).
+    x = np.random.default_rng(6).standard_normal((3, 41)).astype(np.float32) * 5
+    got = oracle_lib.stored_output(x, "bf16")
+    want = fa_inputs.bf16_to_f32(fa_inputs.bf16_bits(x)).astype(np.float64)
+    assert got.shape == x.shape and np.array_equal(got, want)
+    assert np.array_equal(oracle_lib.stored_output(x, "f32"), x.astype(np.float64))
+    y = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 300.5, 0.0, -2.5])
+    assert np.array_equal(oracle_lib.stored_output(y, "bf16"),
+                          [1.0, 1.0 + 2.0 ** -6, 300.0, 0.0, -2.5])
+    assert np.array_equal(oracle_lib.stored_output(y, "exact"), y)
+
+
+def test_stored_output_is_what_the_backward_forms_d_from(oracle_lib):
+    B, H, N, d = 1, 2, 9, 8
+    q, k, v, do = _rand(34, B, H, N, d)
+    o, _ = oracle_lib.attention_fwd(q, k, v, True, 0.5)
+    *_, dvec = oracle_lib.attention_bwd(q, k, v, do, True, 0.5, o_storage="bf16")
+    ob = oracle_lib.stored_output(o, "bf16")
+    want = (do.astype(np.float64) * ob).sum(axis=3).reshape(B * H, N)
+    assert np.max(np.abs(dvec - want)) <= 1e-12
+
+
 def test_stored_output_d(oracle_lib):
     B, H, N, d = 1, 1, 7, 6
     q, k, v, do = _rand(32, B, H, N, d)
@@ -528,6 +554,37 @@ def test_tile_quantisation_bounds_and_independence(oracle_lib):
     c2, s2 = oracle_lib.quantize_e4m3_tiles(y)
     assert np.array_equal(c2, codes)
     assert s2[0, 1, 0] == 8.0 * scales[0, 1, 0] and np.array_equal(s2[0, :, 1:], scales[0, :, 1:])
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if len(line) == 2:
+                vals[line[0]] = int(line[1], 0)
+    return vals
+
+
+def test_tile_scale_rule_on_a_hand_worked_tile(oracle_lib):
+    # tests/golden/fp8_scale_rule.txt: a tile whose code differs between
+    # x * (448 / amax) and x / (amax / 448); the fixture's float32 steps are
+    # re-derived here with IEEE float32 arithmetic before the oracle is asked.
+    g = _golden("fp8_scale_rule.txt")
+    f32 = lambda bits: np.uint32(bits).view(np.float32)  # noqa: E731
+    amax, xv = f32(g["amax_bits"]), f32(g["x_bits"])
+    m = np.float32(np.float32(448.0) / amax)
+    assert m.view(np.uint32) == g["m_bits"]
+    assert np.float32(xv * m).view(np.uint32) == g["product_bits"]
+    assert np.float32(xv / np.float32(amax / np.float32(448.0))) == 92.0
+    tile = np.zeros((1, 1, 128, 64), np.float32)
+    tile[0, 0, 0, 0] = amax
+    tile[0, 0, 5, 7] = xv
+    codes, scales = oracle_lib.quantize_e4m3_tiles(tile)
+    assert codes[0, 0, 0, 0] == 448.0
+    assert codes[0, 0, 5, 7] == g["code_rule_multiply"]
+    assert codes[0, 0, 5, 7] != g["code_rule_divide"]
+    assert scales[0, 0, 0] == np.float32(amax / np.float32(448.0))
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -759,8 +759,8 @@ def kernel_table(fwd_ms, dq_ms, dkdv_ms, f_fwd, f_bwd, step_tflops, burst, mhz):
     and of the datasheet figure, with time x median SM clock beside them.
     The metric's own rates: forward 4 B H N^2 d, backward 2.5x (causal
     halved); a kernel's own rate counts the products it executes."""
-    def row(ms, flops, **extra):
-        tf = flops / (ms * 1e-3) / 1e12
+    def row(ms, work, **extra):
+        tf = work / (ms * 1e-3) / 1e12
         r = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac_of_burst": frac(tf, burst),
              "frac_of_nominal": frac(tf, NOMINAL_BF16_TFLOPS)}
         if mhz:

@@ -63,8 +63,8 @@ namespace fa {
 namespace {
 
 constexpr int kMaxDynSmem = 232448;     // 227 KB opt-in limit per block
-constexpr uint32_t kRegsLight = 64;     // warpgroups 0 and 3 after the split
-constexpr uint32_t kRegsMath = 192;     // warpgroups 1 and 2 after the split
+constexpr uint32_t kRegsLight = 72;     // warpgroups 0 and 3 after the split (no spills)
+constexpr uint32_t kRegsMath = 184;     // warpgroups 1 and 2 after the split
 static_assert(128 * (2 * kRegsLight + 2 * kRegsMath) <= 512 * 128, "register split");
 
 template <int D>

@@ -62,10 +62,10 @@ def kernel_src_sha256(name: str) -> str:
 KERNEL_TRAFFIC = {
     "fwd_bf16": {"bytes": 201437696 + 48240640,
                 "src_sha256": "a139f314cd8d4ab45530e24a33c32cc48cbad0241d8d214647d93dd4294b316d"},
-    "bwd_dkdv_bf16": {"bytes": 270639616 + 219129856,
-                     "src_sha256": "dca583ce6a2c38bd31a4694397f3a0981db558d899f19ad09f06b8f831174f36"},
-    "bwd_dq_bf16": {"bytes": 336706560 + 112510976,
-                   "src_sha256": "b674dc93a94af3ee3b680b85db46f53854e8e100b6ee4d9d3475f44c9a9b63a7"},
+    "bwd_dkdv_bf16": {"bytes": 270631936 + 218725888,
+                     "src_sha256": "6f48d7d5919aa59826264a1142b2efec2cb8a059ed553d34b0038eaae99776fe"},
+    "bwd_dq_bf16": {"bytes": 336653312 + 111471104,
+                   "src_sha256": "a151369f758d3a826a996d484f59264857b0360ffa6be57da0dc1204940f2a69"},
 }
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps
@@ -831,7 +831,7 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
-CASES = ("fp8_quantize", "fp8_forward", "decode")
+CASES = ("step", "fp8_quantize", "fp8_forward", "decode")
 
 
 def run_case(args):
@@ -852,7 +852,26 @@ def run_case(args):
         return torch.randn(*shape, generator=gen, device=dev).to(torch.bfloat16)
 
     scale = fa.default_scale(D)
-    if args.case in ("fp8_quantize", "fp8_forward"):
+    if args.case == "step":
+        # The training step's three kernels on seeded device inputs of the
+        # training-step shape: forward, dQ with the first backward step, dK/dV.
+        q, k, v, do = rnd(B, H, N, D), rnd(B, H, N, D), rnd(B, H, N, D), rnd(B, H, N, D)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = (torch.empty((B, H, N, D), dtype=torch.float32, device=dev)
+                      for _ in range(3))
+        n_pad = (N + 127) // 128 * 128
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, D) // 4, dtype=torch.float32,
+                         device=dev)
+        delta = ws[:B * H * n_pad].view(B * H, n_pad)
+        lse2 = ws[B * H * n_pad:].view(B * H, n_pad)
+        workload = WORKLOAD + " (device-drawn inputs)"
+
+        def fn():
+            fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream)
+            fa.fa_bwd_dq_preprocess(q, k, v, o, do, lse, delta, lse2, dq, CAUSAL, scale, stream)
+            fa.fa_bwd_dkdv(q, k, v, do, delta, lse2, dk, dv, CAUSAL, scale, stream)
+    elif args.case in ("fp8_quantize", "fp8_forward"):
         q, k, v = rnd(B, H, N, D), rnd(B, H, N, D), rnd(B, H, N, D)
         signs = fa._lib._host_signs(fa_inputs.random_signs(SEED, D), D)
         q8, qs = fa.fp8_quantize(q, signs, stream)

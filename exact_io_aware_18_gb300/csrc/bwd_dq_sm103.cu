@@ -12,8 +12,10 @@
 // (no atomics; "FlashAttention-2" stresses a deterministic exact result).
 //
 // Roles (384 threads, one CTA per SM):
-//   warp 0      TMA producer: Q_i and dO_i once, then K_j into a three-deep
-//               ring (K_j is read until the dQ MMA of tile j).
+//   warp 0      TMA producer: (given O) the O tile into the third K stage
+//               first, then Q_i and dO_i once, then K_j into a three-deep ring
+//               (K_j is read until the dQ MMA of tile j); K_2 waits until the
+//               math warps have read O.
 //   warp 11     TMA producer: V_j into a two-deep ring (read only by dP_j).
 //               The two rings free at different times, so each has its own
 //               thread, and each thread its own warp: two lanes of one warp
@@ -29,9 +31,12 @@
 //               ends.
 //   warps 2..9  thread (r, h) owns query row r (TMEM lane r) and key half h.
 //               Given O and LSE, they first do the backward's first step for
-//               their rows (D_r = sum_c dO_rc O_rc from dO in shared memory
-//               and O from global memory, LSE2_r = LSE_r log2 e) and write
-//               D and LSE2 out for the dK/dV kernel; else they read both.
+//               their rows (D_r = sum_c dO_rc O_rc from the dO and O tiles in
+//               shared memory, LSE2_r = LSE_r log2 e) and write D and LSE2 out
+//               for the dK/dV kernel; else they read both.  O comes by TMA like
+//               every other tile: per-thread global loads issued at the start
+//               of a CTA wait behind the streams of K and V tiles of every SM
+//               and took about twice as long to arrive.
 //               Per key tile:
 //               P' = exp2(S * scale*log2e - LSE2_r + log2 scale) = scale P,
 //               dS' = P' o (dP - D_r) = scale dS, BF16, written over the first
@@ -92,7 +97,9 @@ struct DqBars {
     // for dS_j+1; on a single barrier that second phase would hide the first
     // from A's parity wait.  Per buffer, they can be at most one phase ahead.
     static constexpr int DS_FULL = DP_EMPTY + 1;  // 2
-    static constexpr int DQ_DONE = DS_FULL + 2;
+    static constexpr int O_FULL = DS_FULL + 2;
+    static constexpr int O_FREE = O_FULL + 1;
+    static constexpr int DQ_DONE = O_FREE + 1;
     static constexpr int DONE = DQ_DONE + 1;
     static constexpr int COUNT = DONE + 1;
 };
@@ -104,7 +111,8 @@ __global__ void __launch_bounds__(384, 1)
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dq,
-                       const uint4* __restrict__ o, const float* __restrict__ lse,
+                       const __grid_constant__ CUtensorMap tm_o, int fused,
+                       const float* __restrict__ lse,
                        float* __restrict__ delta, float* __restrict__ lse2, int N, int n_pad, int BH,
                        int Hq, int n_rep, int n_tiles, int group,
                        float scale, float scale_log2, unsigned int* status,
@@ -159,6 +167,8 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(bar(Bar::DP_EMPTY), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::DS_FULL), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::DS_FULL + 1), C::COMPUTE_WARPS);
+        mbar_init(bar(Bar::O_FULL), 1);
+        mbar_init(bar(Bar::O_FREE), 1);
         mbar_init(bar(Bar::DQ_DONE), 1);
         mbar_init(bar(Bar::DONE), 2);
         *abort_flag = 0;
@@ -167,6 +177,7 @@ __global__ void __launch_bounds__(384, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_do);
+        if (fused) prefetch_tensormap(&tm_o);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -182,6 +193,15 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producers
         if (lane == 0) {
+            // O first (fused first step): it is on the math warps' path to
+            // their first dS.  It lands in K stage 2, free until K_2.
+            const uint32_t s_o = s_k + 2 * C::TILE_BYTES;
+            if (fused) {
+                mbar_arrive_expect_tx(bar(Bar::O_FULL), C::TILE_BYTES);
+                for (int kb = 0; kb < C::KB; ++kb)
+                    tma_load_3d(s_o + kb * C::BOX_BYTES, &tm_o, bar(Bar::O_FULL), kb * 64,
+                                qt * C::BM, bh);
+            }
             mbar_arrive_expect_tx(bar(Bar::QD_FULL), 2 * C::TILE_BYTES);
             for (int kb = 0; kb < C::KB; ++kb) {
                 tma_load_3d(s_q + kb * C::BOX_BYTES, &tm_q, bar(Bar::QD_FULL), kb * 64,
@@ -193,11 +213,13 @@ __global__ void __launch_bounds__(384, 1)
             for (; issued < n_kv; ++issued) {
                 const int st = issued % C::NSK, use = issued / C::NSK;
                 if (use > 0 && !mbar_wait(bar(Bar::K_EMPTY + st), (use - 1) & 1, wc)) break;
+                if (fused && issued == 2 && !mbar_wait(bar(Bar::O_FREE), 0, wc)) break;
                 mbar_arrive_expect_tx(bar(Bar::K_FULL + st), C::TILE_BYTES);
                 for (int kb = 0; kb < C::KB; ++kb)
                     tma_load_3d(s_k + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_k,
                                 bar(Bar::K_FULL + st), kb * 64, issued * C::BN, bkv);
             }
+            if (fused) mbar_wait_drain(bar(Bar::O_FULL), 0, timeout_ns);
             mbar_wait_drain(bar(Bar::QD_FULL), 0, timeout_ns);
             for (int j = (issued > C::NSK ? issued - C::NSK : 0); j < issued; ++j)
                 mbar_wait_drain(bar(Bar::K_FULL + j % C::NSK), (j / C::NSK) & 1, timeout_ns);
@@ -297,63 +319,41 @@ __global__ void __launch_bounds__(384, 1)
         const long long voff = static_cast<long long>(bh) * n_pad + qt * C::BM + r;
         bool ok = true;
         float d_r, l2_r;  // D_r and LSE_r log2(e); 0 and +inf on padding rows
-        if (o != nullptr) {
-            // The first backward step, fused: D_r = sum_c dO_rc O_rc with dO
-            // from the shared tile and O from global memory, LSE2_r from LSE.
-            // Loads are warp-wide: lane l takes 16-byte chunk l % CH of row
-            // i RPI + l / CH of this warp's 32 rows, so each load instruction
-            // reads whole row halves; the chunk sums meet by shuffles, and the
-            // two halves of a row through shared memory.
-            constexpr int CH = D / 16;   // 16-byte chunks in half a row
-            constexpr int RPI = 32 / CH;
-            const int c = lane % CH;
-            const int col0 = h * (D / 2);
+        if (fused) {
+            // The first backward step, fused: D_r = sum_c dO_rc O_rc over this
+            // thread's half row, both tiles in shared memory (128-byte
+            // swizzled boxes of 64 columns); the two halves of a row meet
+            // through shared memory.  Rows past N hold zeros in both tiles.
             const bool real = qglob < N;
-            // LSE goes out with the O loads: issued after the exchange, its
-            // latency would delay the first tile.
+            // LSE is issued first, so its latency runs under the tile waits.
             const float lse_r = real ? lse[static_cast<long long>(bh) * N + qglob] : 0.f;
-            uint4 ov[CH];
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::QD_FULL), 0, wc) &&
+                                             mbar_wait(bar(Bar::O_FULL), 0, wc));
+            const uint8_t* o_tile = smem + C::OFF_K + 2 * C::TILE_BYTES;
+            float acc = 0.f;
+            if (ok) {
 #pragma unroll
-            for (int i = 0; i < CH; ++i) {
-                const int row = qt * C::BM + wq * 32 + i * RPI + lane / CH;
-                ov[i] = make_uint4(0u, 0u, 0u, 0u);
-                if (row < N)
-                    ov[i] = o[((static_cast<long long>(bh) * N + row) * D + col0) / 8 + c];
-            }
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::QD_FULL), 0, wc));
-            float part[CH];
+                for (int cc = 0; cc < D / 16; ++cc) {
+                    const int gc = h * (D / 16) + cc;  // 16-byte chunk of the row
+                    const int off = (gc >> 3) * C::BOX_BYTES + r * 128 + (((gc & 7) ^ (r & 7)) << 4);
+                    const uint4 ov = *reinterpret_cast<const uint4*>(o_tile + off);
+                    const uint4 dv = *reinterpret_cast<const uint4*>(smem + C::OFF_DO + off);
+                    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
 #pragma unroll
-            for (int i = 0; i < CH; ++i) {
-                const int rt = wq * 32 + i * RPI + lane / CH;  // row inside the tile
-                const int chunk = (col0 % 64) / 8 + c;         // 16-byte chunk inside the box
-                const uint4 dv = *reinterpret_cast<const uint4*>(
-                    smem + C::OFF_DO + (col0 / 64) * C::BOX_BYTES + rt * 128 +
-                    ((chunk ^ (rt & 7)) << 4));
-                const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ov[i]);
-                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
-                float acc = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x = __bfloat1622float2(a2[e]);
-                    const float2 y = __bfloat1622float2(b2[e]);
-                    acc = fmaf(x.x, y.x, acc);
-                    acc = fmaf(x.y, y.y, acc);
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x = __bfloat1622float2(a2[e]);
+                        const float2 y = __bfloat1622float2(b2[e]);
+                        acc = fmaf(x.x, y.x, acc);
+                        acc = fmaf(x.y, y.y, acc);
+                    }
                 }
-#pragma unroll
-                for (int off = CH / 2; off > 0; off >>= 1)
-                    acc += __shfl_xor_sync(0xffffffffu, acc, off);
-                part[i] = acc;
-            }
-            // Lane L owns row L: load i = L / RPI, any lane of group L % RPI.
-            float mine = 0.f;
-#pragma unroll
-            for (int i = 0; i < CH; ++i) {
-                const float t = __shfl_sync(0xffffffffu, part[i], (lane % RPI) * CH);
-                if (i == lane / RPI) mine = t;
             }
             float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
-            xch[h * C::BM + r] = mine;
+            xch[h * C::BM + r] = acc;
             ok = named_bar_and(1, 32 * C::COMPUTE_WARPS, ok);
+            // Every math warp has read O: K_2 may take its stage.
+            if (warp == 2 && lane == 0) mbar_arrive(bar(Bar::O_FREE));
             d_r = real ? xch[r] + xch[C::BM + r] : 0.f;
             l2_r = real ? lse_r * 1.4426950408889634f : INFINITY;
             if (h == 0) {
@@ -461,8 +461,10 @@ cudaError_t launch_t(const DqArgs& a, cudaStream_t stream) {
     int group = 128 / n_tiles;
     if (group < 1) group = 1;
     dim3 grid(n_tiles, a.H, a.B);
+    const bool fused = a.o != nullptr;
     e = launch_overlapped(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tm_q, *a.tm_k,
-                          *a.tm_v, *a.tm_do, *a.tm_dq, static_cast<const uint4*>(a.o), a.lse,
+                          *a.tm_v, *a.tm_do, *a.tm_dq, fused ? *a.tm_o : *a.tm_q,
+                          fused ? 1 : 0, a.lse,
                           a.delta, a.lse2, a.N, a.n_pad, a.B * a.H, a.H, a.H / a.Hkv, n_tiles,
                           group, a.scale, a.scale_log2, a.status, a.timeout_ns);
     return e != cudaSuccess ? e : cudaGetLastError();

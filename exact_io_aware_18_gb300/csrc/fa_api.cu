@@ -247,13 +247,15 @@ int dq_impl(const void* q, const void* k, const void* v, const void* o, const vo
     if (int rc = status_ptr(&status)) return rc;
     const long long BH = static_cast<long long>(B) * Hq;
     const long long BHkv = static_cast<long long>(B) * Hkv;
-    CUtensorMap tq, tk, tv, tdo, tdq;
+    CUtensorMap tq, tk, tv, tdo, tdq, to;
     if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tk, k, d, N, BHkv)) return rc;
     if (int rc = make_map_bf16(&tv, v, d, N, BHkv)) return rc;
     if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
     if (int rc = make_map_f32_out(&tdq, dq, d, N, BH)) return rc;
-    fa::DqArgs a{&tq, &tk, &tv, &tdo, &tdq, o, lse, delta_ws, lse2_ws, B, Hq, N, d,
+    if (o)
+        if (int rc = make_map_bf16(&to, o, d, N, BH)) return rc;
+    fa::DqArgs a{&tq, &tk, &tv, &tdo, &tdq, o, o ? &to : nullptr, lse, delta_ws, lse2_ws, B, Hq, N, d,
                  static_cast<int>(n_pad_of(N)), Hkv, causal ? 1 : 0, scale,
                  scale * 1.4426950408889634f, status, g_timeout_ns.load()};
     return launch_rc(fa::launch_bwd_dq_bf16(a, static_cast<cudaStream_t>(stream)));

@@ -151,8 +151,10 @@ struct DqArgs {
     const CUtensorMap* tm_dq;
     // o (bf16 [B,H,N,d]) and lse (float [B,H,N]) non-null: the kernel also
     // does the first backward step and writes delta and lse2; null: it reads
-    // them as that step wrote them.
+    // them as that step wrote them.  tm_o views o like tm_q views q (null
+    // when o is).
     const void* o;
+    const CUtensorMap* tm_o;
     const float* lse;
     float* delta;
     float* lse2;

@@ -21,9 +21,11 @@
 // the next item's K, V and first [Q | dO] stages load while the current one
 // finishes, and a warpgroup of its own writes the finished dK, dV out of TMEM
 // while the next item computes.
-//   warp 0      TMA producer: K_j, V_j per item (once the last MMAs that read
-//               the previous ones have finished); per Q tile, a two-deep ring
-//               of [Q_i | dO_i] stages plus the 128-entry LSE2 / D vectors.
+//   warp 0      TMA producer: K_j per item once issuer A's last S^T of the
+//               previous item has finished, then the item's first [Q_i | dO_i]
+//               stage, then V_j once issuer B's last dP^T has; per Q tile, a
+//               two-deep ring of [Q_i | dO_i] stages plus the 128-entry LSE2 /
+//               D vectors.
 //   warps 1, 2  two MMA issuers (one thread each).  A single thread issues a
 //               128 x 128 x 16 tcgen05.mma about as fast as the tensor pipe
 //               runs it, so with two issuers one keeps the pipe fed while the
@@ -99,9 +101,14 @@ struct BwdCfg {
 
 template <int NSQ, int QUEUE>
 struct BwdBars {
-    static constexpr int KV_FULL = 0;
-    static constexpr int KV_EMPTY = KV_FULL + 1;
-    static constexpr int Q_FULL = KV_EMPTY + 1;
+    // K and V are reloaded separately: K is free once issuer A's last S^T
+    // of an item has finished, V once issuer B's last dP^T has, about one
+    // MMA group later.
+    static constexpr int K_FULL = 0;
+    static constexpr int V_FULL = K_FULL + 1;
+    static constexpr int K_EMPTY = V_FULL + 1;
+    static constexpr int V_EMPTY = K_EMPTY + 1;
+    static constexpr int Q_FULL = V_EMPTY + 1;
     static constexpr int Q_EMPTY = Q_FULL + NSQ;
     static constexpr int S_FULL = Q_EMPTY + NSQ;
     static constexpr int DP_FULL = S_FULL + 1;
@@ -177,8 +184,10 @@ __global__ void __launch_bounds__(512, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(Bar::KV_FULL), 1);
-        mbar_init(bar(Bar::KV_EMPTY), 2);  // one commit per issuer
+        mbar_init(bar(Bar::K_FULL), 1);
+        mbar_init(bar(Bar::V_FULL), 1);
+        mbar_init(bar(Bar::K_EMPTY), 1);  // issuer A's last S^T of the item
+        mbar_init(bar(Bar::V_EMPTY), 1);  // issuer B's last dP^T of the item
         for (int s = 0; s < C::NSQ; ++s) {
             mbar_init(bar(Bar::Q_FULL + s), 1);
             mbar_init(bar(Bar::Q_EMPTY + s), 2);  // one commit per issuer
@@ -276,24 +285,22 @@ __global__ void __launch_bounds__(512, 1)
         } else if (warp == 0) {
             // ------------------------------------------------------------ producer
             if (lane == 0) {
-                int g = 0, issued = 0, kv_loads = 0;
+                int g = 0, issued = 0, k_loads = 0, v_loads = 0;
                 bool ok = true;
                 for (int k = 0; ok; ++k) {
                     const int item = take_item(k);
                     if (item < 0) break;
                     const Work w = work_of(item);
-                    // K, V of this item once the last MMAs that read the previous
-                    // item's have finished.
-                    if (k >= 1) ok = mbar_wait(bar(Bar::KV_EMPTY), (k - 1) & 1, wc);
+                    // K of this item once issuer A's last S^T of the previous
+                    // item has finished; V (below, after the item's first
+                    // [Q | dO] stage) once issuer B's last dP^T has.
+                    if (k >= 1) ok = mbar_wait(bar(Bar::K_EMPTY), (k - 1) & 1, wc);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(bar(Bar::KV_FULL), 2 * C::TILE_BYTES);
-                    for (int kb = 0; kb < C::KB; ++kb) {
-                        tma_load_3d(s_k + kb * C::BOX_BYTES, &tm_k, bar(Bar::KV_FULL), kb * 64,
+                    mbar_arrive_expect_tx(bar(Bar::K_FULL), C::TILE_BYTES);
+                    for (int kb = 0; kb < C::KB; ++kb)
+                        tma_load_3d(s_k + kb * C::BOX_BYTES, &tm_k, bar(Bar::K_FULL), kb * 64,
                                     w.kt * C::BN, w.bkv);
-                        tma_load_3d(s_v + kb * C::BOX_BYTES, &tm_v, bar(Bar::KV_FULL), kb * 64,
-                                    w.kt * C::BN, w.bkv);
-                    }
-                    kv_loads = k + 1;
+                    k_loads = k + 1;
                     for (int t = 0; t < w.n_steps && ok; ++t, ++g) {
                         const int st = g % C::NSQ;
                         const int use = g / C::NSQ;
@@ -313,12 +320,23 @@ __global__ void __launch_bounds__(512, 1)
                         bulk_load(s_vec + st * 1024, lse2 + voff, 512, fb);
                         bulk_load(s_vec + st * 1024 + 512, delta + voff, 512, fb);
                         issued = g + 1;
+                        if (t == 0) {
+                            if (k >= 1) ok = mbar_wait(bar(Bar::V_EMPTY), (k - 1) & 1, wc);
+                            if (!ok) break;
+                            mbar_arrive_expect_tx(bar(Bar::V_FULL), C::TILE_BYTES);
+                            for (int kb = 0; kb < C::KB; ++kb)
+                                tma_load_3d(s_v + kb * C::BOX_BYTES, &tm_v, bar(Bar::V_FULL),
+                                            kb * 64, w.kt * C::BN, w.bkv);
+                            v_loads = k + 1;
+                        }
                     }
                     if (ok) mbar_arrive(bar(Bar::CLAIM_OK));  // the next item may be claimed
                 }
                 // Drain: no copy may still be landing when the CTA exits.
-                if (kv_loads > 0)
-                    mbar_wait_drain(bar(Bar::KV_FULL), (kv_loads - 1) & 1, timeout_ns);
+                if (k_loads > 0)
+                    mbar_wait_drain(bar(Bar::K_FULL), (k_loads - 1) & 1, timeout_ns);
+                if (v_loads > 0)
+                    mbar_wait_drain(bar(Bar::V_FULL), (v_loads - 1) & 1, timeout_ns);
                 for (int t = (issued > C::NSQ ? issued - C::NSQ : 0); t < issued; ++t)
                     mbar_wait_drain(bar(Bar::Q_FULL + t % C::NSQ), (t / C::NSQ) & 1, timeout_ns);
             }
@@ -365,9 +383,11 @@ __global__ void __launch_bounds__(512, 1)
                     const int item = take_item(k);
                     if (item < 0) break;
                     const Work w = work_of(item);
-                    ok = mbar_wait(bar(Bar::KV_FULL), k & 1, wc) && issue_first(g);
+                    const int kv_full = issuer_a ? Bar::K_FULL : Bar::V_FULL;
+                    const int kv_empty = issuer_a ? Bar::K_EMPTY : Bar::V_EMPTY;
+                    ok = mbar_wait(bar(kv_full), k & 1, wc) && issue_first(g);
                     // K (V) is read for the last time by the item's last first GEMM.
-                    if (ok && w.n_steps == 1) tc_commit(bar(Bar::KV_EMPTY));
+                    if (ok && w.n_steps == 1) tc_commit(bar(kv_empty));
                     for (int t = 0; t < w.n_steps && ok; ++t, ++g) {
                         const int st = g % C::NSQ;
                         ok = mbar_wait(bar(ready_bar), g & 1, wc);
@@ -396,7 +416,7 @@ __global__ void __launch_bounds__(512, 1)
                         tc_commit(bar(Bar::Q_EMPTY + st));  // this issuer no longer reads stage g
                         if (t + 1 < w.n_steps) {
                             ok = issue_first(g + 1);
-                            if (ok && t + 2 == w.n_steps) tc_commit(bar(Bar::KV_EMPTY));
+                            if (ok && t + 2 == w.n_steps) tc_commit(bar(kv_empty));
                         }
                     }
                     if (ok) tc_commit(bar(Bar::ACC_FULL));

@@ -24,26 +24,28 @@
 //               128 x 128 x 16 MMA no faster than the pipe runs it, so its
 //               barrier checks would idle the pipe).  Issuer A: S_0, S_1, then
 //               per key tile j: dQ += dS_j K_j (A = dS_j in TMEM, after
-//               DS_FULL) and S_j+2 = Q K_j+2^T over dS_j.  Issuer B: dP_0, then
+//               DS_FULL) and S_j+2 = Q K_j+2^T over dS_j.  Issuer B: (given O)
+//               D = diag(dO O^T) into the dQ columns, dP_0, then
 //               dP_j+1 = dO V_j+1^T as soon as the math warps hold dP_j in
 //               registers.  S is double buffered and dP is released early, so
 //               both operands of tile j+1 are ready when the math of tile j
 //               ends.
 //   warps 2..9  thread (r, h) owns query row r (TMEM lane r) and key half h.
-//               Given O and LSE, they first do the backward's first step for
-//               their rows (D_r = sum_c dO_rc O_rc from the dO and O tiles in
-//               shared memory, LSE2_r = LSE_r log2 e) and write D and LSE2 out
-//               for the dK/dV kernel; else they read both.  O comes by TMA like
-//               every other tile: per-thread global loads issued at the start
-//               of a CTA wait behind the streams of K and V tiles of every SM
-//               and took about twice as long to arrive.
+//               Given O and LSE, the backward's first step for their rows
+//               comes first: D_r = sum_c dO_rc O_rc is the diagonal of dO O^T,
+//               which issuer B computes on the tensor core into the dQ
+//               columns before any dP (O arrives by TMA in the third K stage);
+//               each thread reads its diagonal entry and writes D and
+//               LSE2_r = LSE_r log2 e out for the dK/dV kernel.  Else they
+//               read both.
 //               Per key tile:
 //               P' = exp2(S * scale*log2e - LSE2_r + log2 scale) = scale P,
 //               dS' = P' o (dP - D_r) = scale dS, BF16, written over the first
 //               32 of its own 64 S columns.  At the end: the dQ row half out
 //               of TMEM into swizzled shared-memory boxes, then to global
 //               memory (FP32) by TMA stores of whole 128-byte rows.
-// TMEM columns: S buffers [0,128) and [128,256), dP [256,384), dQ [384,384+d).
+// TMEM columns: S buffers [0,128) and [128,256), dP [256,384), dQ [384,384+d)
+// (dO O^T takes [384,512) before the first dQ product).
 // All waits are bounded (see sm103_primitives.cuh).
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
@@ -68,8 +70,7 @@ struct DqCfg {
     static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_V + NSV * TILE_BYTES;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int OFF_XCH = OFF_BAR + BAR_BYTES;  // float [2][128]: D halves
-    static constexpr int LAYOUT_BYTES = OFF_XCH + 2 * BM * 4;
+    static constexpr int LAYOUT_BYTES = OFF_BAR + BAR_BYTES;
     static constexpr int SMEM_BYTES =
         (LAYOUT_BYTES + 1024 <= kMaxDynSmem) ? LAYOUT_BYTES + 1024 : kMaxDynSmem;
     static_assert(LAYOUT_BYTES <= kMaxDynSmem, "dQ tiles do not fit in shared memory");
@@ -99,7 +100,8 @@ struct DqBars {
     static constexpr int DS_FULL = DP_EMPTY + 1;  // 2
     static constexpr int O_FULL = DS_FULL + 2;
     static constexpr int O_FREE = O_FULL + 1;
-    static constexpr int DQ_DONE = O_FREE + 1;
+    static constexpr int D_FULL = O_FREE + 1;
+    static constexpr int DQ_DONE = D_FULL + 1;
     static constexpr int DONE = DQ_DONE + 1;
     static constexpr int COUNT = DONE + 1;
 };
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(bar(Bar::DS_FULL + 1), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::O_FULL), 1);
         mbar_init(bar(Bar::O_FREE), 1);
+        mbar_init(bar(Bar::D_FULL), 1);
         mbar_init(bar(Bar::DQ_DONE), 1);
         mbar_init(bar(Bar::DONE), 2);
         *abort_flag = 0;
@@ -304,7 +307,27 @@ __global__ void __launch_bounds__(384, 1)
                 tc_commit(bar(Bar::DP_FULL));
                 return true;
             };
-            bool ok = mbar_wait(bar(Bar::QD_FULL), 0, wc) && issue_dp(0);
+            bool ok = mbar_wait(bar(Bar::QD_FULL), 0, wc);
+            if (ok && fused) {
+                // The first backward step on the tensor core: dO O^T into the
+                // dQ columns (free until the first dQ product), whose
+                // diagonal is D_r = sum_c dO_rc O_rc.  Both operands K-major,
+                // O in the K stage it arrived in.
+                ok = mbar_wait(bar(Bar::O_FULL), 0, wc);
+                if (ok) {
+                    tc_fence_after();
+                    const uint64_t d_o = smem_desc_sw128(s_k + 2 * C::TILE_BYTES, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                        mma_ss(tmem + C::COL_DQ, desc_advance(d_do, koff),
+                               desc_advance(d_o, koff), id_p, kk > 0);
+                    }
+                    tc_commit(bar(Bar::D_FULL));
+                    tc_commit(bar(Bar::O_FREE));  // O has been read: K_2 may take its stage
+                }
+            }
+            ok = ok && issue_dp(0);
             for (int j = 0; j + 1 < n_kv && ok; ++j)  // the math warps hold dP_j in registers
                 ok = mbar_wait(bar(Bar::DP_EMPTY), j & 1, wc) && issue_dp(j + 1);
         }
@@ -320,41 +343,24 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
         float d_r, l2_r;  // D_r and LSE_r log2(e); 0 and +inf on padding rows
         if (fused) {
-            // The first backward step, fused: D_r = sum_c dO_rc O_rc over this
-            // thread's half row, both tiles in shared memory (128-byte
-            // swizzled boxes of 64 columns); the two halves of a row meet
-            // through shared memory.  Rows past N hold zeros in both tiles.
+            // The first backward step, fused: D_r is the diagonal entry
+            // (r, r) of dO O^T, which issuer B computes into the dQ columns;
+            // lane r of this warp's quarter finds it at column r.
             const bool real = qglob < N;
-            // LSE is issued first, so its latency runs under the tile waits.
+            // LSE is issued first, so its latency runs under the waits.
             const float lse_r = real ? lse[static_cast<long long>(bh) * N + qglob] : 0.f;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::QD_FULL), 0, wc) &&
-                                             mbar_wait(bar(Bar::O_FULL), 0, wc));
-            const uint8_t* o_tile = smem + C::OFF_K + 2 * C::TILE_BYTES;
-            float acc = 0.f;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::D_FULL), 0, wc));
+            float dg = 0.f;
             if (ok) {
+                tc_fence_after();
+                uint32_t a[32];
+                tmem_ld32(t_lane + C::COL_DQ + 32 * wq, a);
 #pragma unroll
-                for (int cc = 0; cc < D / 16; ++cc) {
-                    const int gc = h * (D / 16) + cc;  // 16-byte chunk of the row
-                    const int off = (gc >> 3) * C::BOX_BYTES + r * 128 + (((gc & 7) ^ (r & 7)) << 4);
-                    const uint4 ov = *reinterpret_cast<const uint4*>(o_tile + off);
-                    const uint4 dv = *reinterpret_cast<const uint4*>(smem + C::OFF_DO + off);
-                    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 x = __bfloat1622float2(a2[e]);
-                        const float2 y = __bfloat1622float2(b2[e]);
-                        acc = fmaf(x.x, y.x, acc);
-                        acc = fmaf(x.y, y.y, acc);
-                    }
-                }
+                for (int i = 0; i < 32; ++i)
+                    if (i == lane) dg = __uint_as_float(a[i]);
+                tc_fence_before();
             }
-            float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
-            xch[h * C::BM + r] = acc;
-            ok = named_bar_and(1, 32 * C::COMPUTE_WARPS, ok);
-            // Every math warp has read O: K_2 may take its stage.
-            if (warp == 2 && lane == 0) mbar_arrive(bar(Bar::O_FREE));
-            d_r = real ? xch[r] + xch[C::BM + r] : 0.f;
+            d_r = real ? dg : 0.f;
             l2_r = real ? lse_r * 1.4426950408889634f : INFINITY;
             if (h == 0) {
                 delta[voff] = d_r;

@@ -496,17 +496,19 @@ __global__ void __launch_bounds__(512, 1)
                     uint32_t sr[64];
                     tmem_ld64(t_lane + C::COL_S + 64 * h, sr);
                     const int q0 = i * C::BM + 64 * h;  // query index of entry 0
+                    const float2 c2 = make_float2(scale_log2, scale_log2);
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        const float2 x = fma2(make_float2(__uint_as_float(sr[c]),
+                                                          __uint_as_float(sr[c + 1])),
+                                              c2, make_float2(-l2v[c], -l2v[c + 1]));
+                        p[c] = ex2_approx(x.x);
+                        p[c + 1] = ex2_approx(x.y);
+                    }
                     if (key_pad || (CAUSAL && i == w.kt)) {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            const float x =
-                                ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, -l2v[c]));
-                            p[c] = (key_pad || q0 + c < kglob) ? 0.f : x;
-                        }
-                    } else {
-#pragma unroll
                         for (int c = 0; c < 64; ++c)
-                            p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, -l2v[c]));
+                            if (key_pad || q0 + c < kglob) p[c] = 0.f;
                     }
                 }
                 {
@@ -528,11 +530,16 @@ __global__ void __launch_bounds__(512, 1)
                     uint32_t dr[64];
                     tmem_ld64(t_lane + C::COL_DP + 64 * h, dr);
                     uint32_t wv[32];
+                    const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int c = 2 * e;
-                        wv[e] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - dlt[c]),
-                                            p[c + 1] * (__uint_as_float(dr[c + 1]) - dlt[c + 1]));
+                        // dP - D exactly as a subtraction (D * -1 is exact), then P o (dP - D).
+                        const float2 t = fma2(make_float2(dlt[c], dlt[c + 1]), m1,
+                                              make_float2(__uint_as_float(dr[c]),
+                                                          __uint_as_float(dr[c + 1])));
+                        const float2 ds = mul2(make_float2(p[c], p[c + 1]), t);
+                        wv[e] = pack_bf16x2(ds.x, ds.y);
                     }
                     tmem_st32(t_lane + C::COL_DP + 64 * h, wv);
                 }

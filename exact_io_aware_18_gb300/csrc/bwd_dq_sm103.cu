@@ -372,6 +372,9 @@ __global__ void __launch_bounds__(384, 1)
         }
         // P = 0 on padding rows (l2_r = +inf); log2(scale) folds scale into P.
         const float neg_l2 = log2f(scale) - l2_r;
+        const float2 c2 = make_float2(scale_log2, scale_log2);
+        const float2 neg_l2_2 = make_float2(neg_l2, neg_l2);
+        const float2 neg_d2 = make_float2(-d_r, -d_r);  // dP - D as an addition of -D
         for (int j = 0; ok && j < n_kv; ++j) {
             const uint32_t t_s = t_lane + ((j & 1) ? C::COL_S1 : C::COL_S0) + 64 * h;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_FULL + (j & 1)), (j >> 1) & 1, wc) &&
@@ -392,18 +395,21 @@ __global__ void __launch_bounds__(384, 1)
                 tmem_ld32(t_s + 32 * ch, sr);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    float ds[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int c = 2 * e + u;
-                        float p = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, neg_l2));
-                        if (masked) {
-                            const int key = key0 + 32 * ch + c;
-                            if ((CAUSAL && key > qglob) || key >= N) p = 0.f;
-                        }
-                        ds[u] = p * (__uint_as_float(dr[32 * ch + c]) - d_r);
+                    const int c = 2 * e;
+                    const float2 x = fma2(make_float2(__uint_as_float(sr[c]),
+                                                      __uint_as_float(sr[c + 1])),
+                                          c2, neg_l2_2);
+                    float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    if (masked) {
+                        const int key = key0 + 32 * ch + c;
+                        if ((CAUSAL && key > qglob) || key >= N) p.x = 0.f;
+                        if ((CAUSAL && key + 1 > qglob) || key + 1 >= N) p.y = 0.f;
                     }
-                    w[e] = pack_bf16x2(ds[0], ds[1]);
+                    const float2 t = add2(make_float2(__uint_as_float(dr[32 * ch + c]),
+                                                      __uint_as_float(dr[32 * ch + c + 1])),
+                                          neg_d2);
+                    const float2 ds = mul2(p, t);
+                    w[e] = pack_bf16x2(ds.x, ds.y);
                 }
                 // Chunk ch's dS lands on S columns [16 ch, 16 ch + 16) of this
                 // half, which chunk 0 has already read.

@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(384, 1)
                         }
                     }
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
+                    for (int c = 0; c < 64; c += 2) mx = fmax3(mx, s[c], s[c + 1]);
                 }
                 xch[(b * 2 + h) * 128 + row] = mx;
                 ok = named_bar_and(pair_bar, 64, okw);
@@ -544,16 +544,18 @@ __global__ void __launch_bounds__(384, 1)
                     alpha = ex2_approx(m_run - m_tile);
                     m_run = m_tile;
                 }
-                const float neg_m = -m_run;
-                float sum = 0.f;
+                const float2 c_s2 = make_float2(c_s, c_s);
+                const float2 neg_m2 = make_float2(-m_run, -m_run);
+                float2 sum2 = make_float2(0.f, 0.f);  // even and odd keys
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2_approx(fmaf(s[2 * e], c_s, neg_m));
-                    const float p1 = ex2_approx(fmaf(s[2 * e + 1], c_s, neg_m));
-                    sum += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
+                    const float2 x = fma2(make_float2(s[2 * e], s[2 * e + 1]), c_s2, neg_m2);
+                    const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    sum2 = add2(sum2, pp);
+                    pk[e] = pack_bf16x2(pp.x, pp.y);
                 }
+                const float sum = sum2.x + sum2.y;
                 l_run = l_run * alpha + sum;
                 if (j > w.j0) {
                     // PV_{j-1} has finished: the P buffer is free, and O holds
@@ -570,9 +572,14 @@ __global__ void __launch_bounds__(384, 1)
                         uint32_t r[32];
                         const uint32_t t_o = t_lane + C::COL_O + (D / 2) * h + c * 32;
                         tmem_ld32(t_o, r);
+                        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 v = mul2(make_float2(__uint_as_float(r[e]),
+                                                              __uint_as_float(r[e + 1])), a2);
+                            r[e] = __float_as_uint(v.x);
+                            r[e + 1] = __float_as_uint(v.y);
+                        }
                         tmem_st32(t_o, r);
                     }
                 }

@@ -497,13 +497,20 @@ __global__ void __launch_bounds__(512, 1)
                     tmem_ld64(t_lane + C::COL_S + 64 * h, sr);
                     const int q0 = i * C::BM + 64 * h;  // query index of entry 0
                     const float2 c2 = make_float2(scale_log2, scale_log2);
+                    const float4* l2v4 = reinterpret_cast<const float4*>(l2v);  // 16-byte broadcasts
 #pragma unroll
-                    for (int c = 0; c < 64; c += 2) {
-                        const float2 x = fma2(make_float2(__uint_as_float(sr[c]),
-                                                          __uint_as_float(sr[c + 1])),
-                                              c2, make_float2(-l2v[c], -l2v[c + 1]));
-                        p[c] = ex2_approx(x.x);
-                        p[c + 1] = ex2_approx(x.y);
+                    for (int c = 0; c < 64; c += 4) {
+                        const float4 l = l2v4[c / 4];
+                        const float2 x0 = fma2(make_float2(__uint_as_float(sr[c]),
+                                                           __uint_as_float(sr[c + 1])),
+                                               c2, make_float2(-l.x, -l.y));
+                        const float2 x1 = fma2(make_float2(__uint_as_float(sr[c + 2]),
+                                                           __uint_as_float(sr[c + 3])),
+                                               c2, make_float2(-l.z, -l.w));
+                        p[c] = ex2_approx(x0.x);
+                        p[c + 1] = ex2_approx(x0.y);
+                        p[c + 2] = ex2_approx(x1.x);
+                        p[c + 3] = ex2_approx(x1.y);
                     }
                     if (key_pad || (CAUSAL && i == w.kt)) {
 #pragma unroll
@@ -531,15 +538,22 @@ __global__ void __launch_bounds__(512, 1)
                     tmem_ld64(t_lane + C::COL_DP + 64 * h, dr);
                     uint32_t wv[32];
                     const float2 m1 = make_float2(-1.f, -1.f);
+                    const float4* dlt4 = reinterpret_cast<const float4*>(dlt);  // 16-byte broadcasts
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
+                    for (int e = 0; e < 32; e += 2) {
                         const int c = 2 * e;
+                        const float4 dd = dlt4[c / 4];
                         // dP - D exactly as a subtraction (D * -1 is exact), then P o (dP - D).
-                        const float2 t = fma2(make_float2(dlt[c], dlt[c + 1]), m1,
-                                              make_float2(__uint_as_float(dr[c]),
-                                                          __uint_as_float(dr[c + 1])));
-                        const float2 ds = mul2(make_float2(p[c], p[c + 1]), t);
-                        wv[e] = pack_bf16x2(ds.x, ds.y);
+                        const float2 t0 = fma2(make_float2(dd.x, dd.y), m1,
+                                               make_float2(__uint_as_float(dr[c]),
+                                                           __uint_as_float(dr[c + 1])));
+                        const float2 t1 = fma2(make_float2(dd.z, dd.w), m1,
+                                               make_float2(__uint_as_float(dr[c + 2]),
+                                                           __uint_as_float(dr[c + 3])));
+                        const float2 ds0 = mul2(make_float2(p[c], p[c + 1]), t0);
+                        const float2 ds1 = mul2(make_float2(p[c + 2], p[c + 3]), t1);
+                        wv[e] = pack_bf16x2(ds0.x, ds0.y);
+                        wv[e + 1] = pack_bf16x2(ds1.x, ds1.y);
                     }
                     tmem_st32(t_lane + C::COL_DP + 64 * h, wv);
                 }

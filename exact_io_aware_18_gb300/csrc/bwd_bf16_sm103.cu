@@ -343,7 +343,9 @@ __global__ void __launch_bounds__(512, 1)
             __syncwarp();
         } else if (warp == 1 || warp == 2) {
             // ------------------------------------------------------------ MMA issuers
-            if (lane == 0) {
+            // Each issuer is a whole warp: every lane waits and computes the
+            // operands, one elected lane issues the MMAs and commits.
+            {
                 constexpr uint32_t id_sp = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
                 constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);    // dV, dK: B MN-major
                 const bool issuer_a = (warp == 1);
@@ -366,63 +368,74 @@ __global__ void __launch_bounds__(512, 1)
                 // First GEMM of step g: S^T = K Q^T (A) or dP^T = V dO^T (B).
                 auto issue_first = [&](int g) -> bool {
                     const int st = g % C::NSQ;
-                    if (!mbar_wait(bar(Bar::Q_FULL + st), (g / C::NSQ) & 1, wc)) return false;
+                    if (!mbar_wait_warp(bar(Bar::Q_FULL + st), (g / C::NSQ) & 1, wc)) return false;
                     tc_fence_after();
+                    const uint64_t d_b = desc_advance(d_kmaj0, st * C::STAGE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                        mma_ss(tmem + c_first, desc_advance(d_first, koff),
-                               desc_advance(d_kmaj0, st * C::STAGE_BYTES + koff), id_sp, kk > 0);
+                        const uint64_t ad = desc_advance(d_first, koff);
+                        const uint64_t bd = desc_advance(d_b, koff);
+                        if (elect_one()) mma_ss(tmem + c_first, ad, bd, id_sp, kk > 0);
+                        __syncwarp();
                     }
-                    tc_commit(bar(full_bar));
+                    if (elect_one()) tc_commit(bar(full_bar));
+                    __syncwarp();
                     return true;
                 };
                 int g = 0;  // step counter across this CTA's items
                 bool ok = true;
                 for (int k = 0; ok; ++k) {
-                    const int item = take_item(k);
+                    const int item = take_item_warp(k);
                     if (item < 0) break;
                     const Work w = work_of(item);
                     const int kv_full = issuer_a ? Bar::K_FULL : Bar::V_FULL;
                     const int kv_empty = issuer_a ? Bar::K_EMPTY : Bar::V_EMPTY;
-                    ok = mbar_wait(bar(kv_full), k & 1, wc) && issue_first(g);
+                    ok = mbar_wait_warp(bar(kv_full), k & 1, wc) && issue_first(g);
                     // K (V) is read for the last time by the item's last first GEMM.
-                    if (ok && w.n_steps == 1) tc_commit(bar(kv_empty));
+                    if (ok && w.n_steps == 1 && elect_one()) tc_commit(bar(kv_empty));
+                    __syncwarp();
                     for (int t = 0; t < w.n_steps && ok; ++t, ++g) {
                         const int st = g % C::NSQ;
-                        ok = mbar_wait(bar(ready_bar), g & 1, wc);
+                        ok = mbar_wait_warp(bar(ready_bar), g & 1, wc);
                         // The item's first accumulation overwrites dV (dK): the
                         // epilogue must have read the previous item's out.
-                        if (ok && t == 0 && k >= 1) ok = mbar_wait(bar(free_bar), (k - 1) & 1, wc);
+                        if (ok && t == 0 && k >= 1) ok = mbar_wait_warp(bar(free_bar), (k - 1) & 1, wc);
                         // Issuer B holds dK_t and dP^T_t+1 until issuer A's S^T_t+1 is
                         // done: A's dV_t, S^T_t+1 lead to the next P phase and should
                         // not share the pipe; B's pair then runs during that P phase.
                         // S_FULL cannot pass step t+1 before this wait: S^T_t+2 needs
                         // the stage that B frees only after dK_t.
                         if (ok && !issuer_a && t + 1 < w.n_steps)
-                            ok = mbar_wait(bar(Bar::S_FULL), (g + 1) & 1, wc);
+                            ok = mbar_wait_warp(bar(Bar::S_FULL), (g + 1) & 1, wc);
                         if (!ok) break;
                         tc_fence_after();
                         // dV += P^T dO (A) or dK += dS^T Q (B); the BF16 halves of
                         // P^T / dS^T (queries 0-63, 64-127) sit at columns [0,32)
                         // and [64,96) of their fp32 region.
+                        const uint64_t d_mn = desc_advance(d_mn0, st * C::STAGE_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < C::BM / 16; ++kk) {
                             const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-                            mma_ts(tmem + c_acc, tmem + c_a + acol,
-                                   desc_advance(d_mn0, st * C::STAGE_BYTES + kk * 2048), id_kv,
-                                   (t > 0 || kk > 0) ? 1u : 0u);
+                            const uint64_t bd = desc_advance(d_mn, kk * 2048);
+                            if (elect_one())
+                                mma_ts(tmem + c_acc, tmem + c_a + acol, bd, id_kv,
+                                       (t > 0 || kk > 0) ? 1u : 0u);
+                            __syncwarp();
                         }
-                        tc_commit(bar(Bar::Q_EMPTY + st));  // this issuer no longer reads stage g
+                        // This issuer no longer reads stage g.
+                        if (elect_one()) tc_commit(bar(Bar::Q_EMPTY + st));
+                        __syncwarp();
                         if (t + 1 < w.n_steps) {
                             ok = issue_first(g + 1);
-                            if (ok && t + 2 == w.n_steps) tc_commit(bar(kv_empty));
+                            if (ok && t + 2 == w.n_steps && elect_one()) tc_commit(bar(kv_empty));
+                            __syncwarp();
                         }
                     }
-                    if (ok) tc_commit(bar(Bar::ACC_FULL));
+                    if (ok && elect_one()) tc_commit(bar(Bar::ACC_FULL));
+                    __syncwarp();
                 }
             }
-            __syncwarp();
         } else {
             // ------------------------------------------------------------ epilogue
             // Warp e (of warps 12-15) owns TMEM lanes 32 (e % 4) .. +32: rows
@@ -567,9 +580,10 @@ __global__ void __launch_bounds__(512, 1)
 
     // ---------------------------------------------------------------- teardown
     __syncthreads();
-    if (warp == 2 && lane == 0) tc_commit(bar(Bar::DONE));
+    // The commits come from the lane that issued each warp's MMAs.
+    if (warp == 2 && elect_one()) tc_commit(bar(Bar::DONE));
     if (warp == 1) {
-        if (lane == 0) {
+        if (elect_one()) {
             tc_commit(bar(Bar::DONE));  // both issuers' MMAs have completed
             mbar_wait_drain(bar(Bar::DONE), 0, timeout_ns);
         }

@@ -245,7 +245,20 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer A
-        if (lane == 0) {
+        // Each issuer is a whole warp: every lane waits and computes the
+        // operands, one elected lane issues the MMAs and commits.  Under a
+        // causal mask issuer A is lane 0 alone instead: measured both ways,
+        // the whole warp made dQ 5 % faster without the mask and 2-3 % slower
+        // with it (the cause was not found).
+        constexpr bool kWarpA = !CAUSAL;
+        auto wait_a = [&](uint32_t b, uint32_t parity) {
+            return kWarpA ? mbar_wait_warp(b, parity, wc) : mbar_wait(b, parity, wc);
+        };
+        auto lead_a = [&]() { return kWarpA ? elect_one() : true; };
+        auto sync_a = [&]() {
+            if (kWarpA) __syncwarp();
+        };
+        if (kWarpA || lane == 0) {
             constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // S: both K-major
             constexpr uint32_t id_q = idesc_bf16(128, D, 0, 1);    // dQ: B MN-major
             const uint64_t d_q = smem_desc_sw128(s_q, 16, 1024);
@@ -253,85 +266,104 @@ __global__ void __launch_bounds__(384, 1)
             const uint64_t d_kmn = smem_desc_sw128(s_k, C::BOX_BYTES, 1024);  // K, MN-major
             auto issue_s = [&](int j) -> bool {  // S_j = Q K_j^T into buffer j & 1
                 const int st = j % C::NSK;
-                if (!mbar_wait(bar(Bar::K_FULL + st), (j / C::NSK) & 1, wc)) return false;
+                if (!wait_a(bar(Bar::K_FULL + st), (j / C::NSK) & 1)) return false;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+                const uint64_t d_b = desc_advance(d_kk, st * C::TILE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                    mma_ss(d_tmem, desc_advance(d_q, koff),
-                           desc_advance(d_kk, st * C::TILE_BYTES + koff), id_s, kk > 0);
+                    const uint64_t ad = desc_advance(d_q, koff);
+                    const uint64_t bd = desc_advance(d_b, koff);
+                    if (lead_a()) mma_ss(d_tmem, ad, bd, id_s, kk > 0);
+                    sync_a();
                 }
-                tc_commit(bar(Bar::S_FULL + (j & 1)));
+                if (lead_a()) tc_commit(bar(Bar::S_FULL + (j & 1)));
+                sync_a();
                 return true;
             };
-            bool ok = mbar_wait(bar(Bar::QD_FULL), 0, wc) && issue_s(0);
+            bool ok = wait_a(bar(Bar::QD_FULL), 0) && issue_s(0);
             if (ok && n_kv > 1) ok = issue_s(1);
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int st = j % C::NSK;
-                ok = mbar_wait(bar(Bar::DS_FULL + (j & 1)), (j >> 1) & 1, wc);
+                ok = wait_a(bar(Bar::DS_FULL + (j & 1)), (j >> 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t s_cols = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+                const uint64_t d_b = desc_advance(d_kmn, st * C::TILE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk) {  // dQ += dS_j K_j
                     // dS halves: keys 0-63 at columns [0,32), 64-127 at [64,96).
                     const uint32_t scol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-                    mma_ts(tmem + C::COL_DQ, s_cols + scol,
-                           desc_advance(d_kmn, st * C::TILE_BYTES + kk * 2048), id_q,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t bd = desc_advance(d_b, kk * 2048);
+                    if (lead_a())
+                        mma_ts(tmem + C::COL_DQ, s_cols + scol, bd, id_q,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                    sync_a();
                 }
-                tc_commit(bar(Bar::K_EMPTY + st));
+                if (lead_a()) tc_commit(bar(Bar::K_EMPTY + st));
+                sync_a();
                 if (j + 2 < n_kv) ok = issue_s(j + 2);
             }
-            if (ok) tc_commit(bar(Bar::DQ_DONE));
+            if (ok && lead_a()) tc_commit(bar(Bar::DQ_DONE));
+            sync_a();
         }
         __syncwarp();
     } else if (warp == 10) {
         // ------------------------------------------------------------ MMA issuer B
-        if (lane == 0) {
+        {
             constexpr uint32_t id_p = idesc_bf16(128, 128, 0, 0);  // dP: both K-major
             const uint64_t d_do = smem_desc_sw128(s_do, 16, 1024);
             const uint64_t d_vv = smem_desc_sw128(s_v, 16, 1024);
             auto issue_dp = [&](int j) -> bool {  // dP_j = dO V_j^T
                 const int st = j % C::NSV;
-                if (!mbar_wait(bar(Bar::V_FULL + st), (j / C::NSV) & 1, wc)) return false;
+                if (!mbar_wait_warp(bar(Bar::V_FULL + st), (j / C::NSV) & 1, wc)) return false;
                 tc_fence_after();
+                const uint64_t d_b = desc_advance(d_vv, st * C::TILE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                    mma_ss(tmem + C::COL_DP, desc_advance(d_do, koff),
-                           desc_advance(d_vv, st * C::TILE_BYTES + koff), id_p, kk > 0);
+                    const uint64_t ad = desc_advance(d_do, koff);
+                    const uint64_t bd = desc_advance(d_b, koff);
+                    if (elect_one()) mma_ss(tmem + C::COL_DP, ad, bd, id_p, kk > 0);
+                    __syncwarp();
                 }
-                tc_commit(bar(Bar::V_EMPTY + st));
-                tc_commit(bar(Bar::DP_FULL));
+                if (elect_one()) {
+                    tc_commit(bar(Bar::V_EMPTY + st));
+                    tc_commit(bar(Bar::DP_FULL));
+                }
+                __syncwarp();
                 return true;
             };
-            bool ok = mbar_wait(bar(Bar::QD_FULL), 0, wc);
+            bool ok = mbar_wait_warp(bar(Bar::QD_FULL), 0, wc);
             if (ok && fused) {
                 // The first backward step on the tensor core: dO O^T into the
                 // dQ columns (free until the first dQ product), whose
                 // diagonal is D_r = sum_c dO_rc O_rc.  Both operands K-major,
                 // O in the K stage it arrived in.
-                ok = mbar_wait(bar(Bar::O_FULL), 0, wc);
+                ok = mbar_wait_warp(bar(Bar::O_FULL), 0, wc);
                 if (ok) {
                     tc_fence_after();
                     const uint64_t d_o = smem_desc_sw128(s_k + 2 * C::TILE_BYTES, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                        mma_ss(tmem + C::COL_DQ, desc_advance(d_do, koff),
-                               desc_advance(d_o, koff), id_p, kk > 0);
+                        const uint64_t ad = desc_advance(d_do, koff);
+                        const uint64_t bd = desc_advance(d_o, koff);
+                        if (elect_one()) mma_ss(tmem + C::COL_DQ, ad, bd, id_p, kk > 0);
+                        __syncwarp();
                     }
-                    tc_commit(bar(Bar::D_FULL));
-                    tc_commit(bar(Bar::O_FREE));  // O has been read: K_2 may take its stage
+                    if (elect_one()) {
+                        tc_commit(bar(Bar::D_FULL));
+                        tc_commit(bar(Bar::O_FREE));  // O has been read: K_2 may take its stage
+                    }
+                    __syncwarp();
                 }
             }
             ok = ok && issue_dp(0);
             for (int j = 0; j + 1 < n_kv && ok; ++j)  // the math warps hold dP_j in registers
-                ok = mbar_wait(bar(Bar::DP_EMPTY), j & 1, wc) && issue_dp(j + 1);
+                ok = mbar_wait_warp(bar(Bar::DP_EMPTY), j & 1, wc) && issue_dp(j + 1);
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ P / dS
         const int wq = warp & 3;
@@ -450,9 +482,10 @@ __global__ void __launch_bounds__(384, 1)
 
     // ---------------------------------------------------------------- teardown
     __syncthreads();
-    if (warp == 10 && lane == 0) tc_commit(bar(Bar::DONE));
+    // The commits come from the lane that issued each warp's MMAs.
+    if (warp == 10 && elect_one()) tc_commit(bar(Bar::DONE));
     if (warp == 1) {
-        if (lane == 0) {
+        if (CAUSAL ? lane == 0 : elect_one()) {
             tc_commit(bar(Bar::DONE));  // both issuers' MMAs have completed
             mbar_wait_drain(bar(Bar::DONE), 0, timeout_ns);
         }

@@ -229,6 +229,15 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(bar(Bar::ITEM_EMPTY + slot));
         return item;
     };
+    // The same for a whole warp (the MMA issuers): one arrival per warp.
+    auto take_item_warp = [&](int k) -> int {
+        const int slot = k % C::QUEUE;
+        if (!mbar_wait_warp(bar(Bar::ITEM_FULL + slot), (k / C::QUEUE) & 1, wc)) return -1;
+        const int item = __shfl_sync(0xffffffffu, items[slot], 0);
+        if (elect_one()) mbar_arrive(bar(Bar::ITEM_EMPTY + slot));
+        __syncwarp();
+        return item;
+    };
 
     // Warpgroup 0 (warps 0-3: one thread each of real work) gives registers
     // to the softmax warpgroups 1 and 2:
@@ -339,84 +348,96 @@ __global__ void __launch_bounds__(384, 1)
             __syncwarp();
         } else {  // warps 1, 2
             // ------------------------------------------------------------ MMA issuers
-            if (lane == 0) {
-                constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // B = K, K-major
-                constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);   // B = V, MN-major
-                int g = 0;  // tile counter across this CTA's Q tiles
-                bool ok = true;
-                for (int k = 0; ok; ++k) {
-                    const int item = take_item(k);
-                    if (item < 0) break;
-                    const Work w = work_of(item);
-                    if (warp == 2) {
-                        // Issuer B: O += P_j V_j as soon as the softmax warps release P_j.
-                        for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
-                            const int st = g % C::NS;
-                            ok = mbar_wait(bar(Bar::P_FULL), g & 1, wc) &&
-                                 mbar_wait(bar(Bar::V_FULL + st), (g / C::NS) & 1, wc);
-                            if (!ok) break;
-                            tc_fence_after();
-                            const uint32_t v_tile = s_v + st * C::TILE_BYTES;
+            // Each issuer is a whole warp: every lane waits and computes the
+            // operands, one elected lane issues the MMAs and commits.
+            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // B = K, K-major
+            constexpr uint32_t id_pv = idesc_bf16(128, D, 0, 1);   // B = V, MN-major
+            int g = 0;  // tile counter across this CTA's Q tiles
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int item = take_item_warp(k);
+                if (item < 0) break;
+                const Work w = work_of(item);
+                if (warp == 2) {
+                    // Issuer B: O += P_j V_j as soon as the softmax warps release P_j.
+                    for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
+                        const int st = g % C::NS;
+                        ok = mbar_wait_warp(bar(Bar::P_FULL), g & 1, wc) &&
+                             mbar_wait_warp(bar(Bar::V_FULL + st), (g / C::NS) & 1, wc);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t v_tile = s_v + st * C::TILE_BYTES;
 #pragma unroll
-                            for (int kk = 0; kk < C::BN / 16; ++kk) {
-                                // V as an MN-major B operand: 16 keys = 2 atoms of 8 rows.
-                                const uint64_t bd =
-                                    smem_desc_sw128(v_tile + kk * 2048, C::BOX_BYTES, 1024);
+                        for (int kk = 0; kk < C::BN / 16; ++kk) {
+                            // V as an MN-major B operand: 16 keys = 2 atoms of 8 rows.
+                            const uint64_t bd =
+                                smem_desc_sw128(v_tile + kk * 2048, C::BOX_BYTES, 1024);
+                            if (elect_one())
                                 mma_ts(tmem + C::COL_O, tmem + C::COL_P + kk * 8, bd, id_pv,
                                        (j > w.j0 || kk > 0));
-                            }
+                            __syncwarp();
+                        }
+                        if (elect_one()) {
                             tc_commit(bar(Bar::V_EMPTY + st));
                             tc_commit(bar(Bar::O_FULL));
                         }
-                    } else {
-                        // Issuer A: S_j = Q K_j^T into buffer g & 1 once the softmax
-                        // warps have read S_{g-2} out of it (the next phase of that
-                        // S_EMPTY needs S_g itself, so the wait cannot miss it).
-                        // Q in TMEM (BF16) or Q's E4M3 tile in shared memory (FP8).
-                        if constexpr (FP8) ok = mbar_wait(bar(Bar::Q_FULL + (k & 1)), (k >> 1) & 1, wc);
-                        else ok = mbar_wait(bar(Bar::QT_FULL), k & 1, wc);
-                        for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
-                            const int st = g % C::NS;
-                            const int b = g & 1;
-                            if (g >= 2) ok = mbar_wait(bar(Bar::S_EMPTY + b), ((g - 2) >> 1) & 1, wc);
-                            ok = ok && mbar_wait(bar(Bar::K_FULL + st), (g / C::NS) & 1, wc);
-                            if (!ok) break;
-                            tc_fence_after();
-                            const uint32_t k_tile = s_k + st * C::QK_BYTES;
-                            const uint32_t d_tmem = tmem + (b ? C::COL_S1 : C::COL_S0);
-                            if constexpr (FP8) {
-                                // E4M3 codes, 32 bytes of K per instruction, both
-                                // operands K-major in shared memory.
-                                constexpr uint32_t id_s8 = idesc_e4m3(128, 128);
-                                const uint32_t q_tile = s_q + (k & 1) * C::TILE_BYTES;
+                        __syncwarp();
+                    }
+                } else {
+                    // Issuer A: S_j = Q K_j^T into buffer g & 1 once the softmax
+                    // warps have read S_{g-2} out of it (the next phase of that
+                    // S_EMPTY needs S_g itself, so the wait cannot miss it).
+                    // Q in TMEM (BF16) or Q's E4M3 tile in shared memory (FP8).
+                    if constexpr (FP8) ok = mbar_wait_warp(bar(Bar::Q_FULL + (k & 1)), (k >> 1) & 1, wc);
+                    else ok = mbar_wait_warp(bar(Bar::QT_FULL), k & 1, wc);
+                    for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
+                        const int st = g % C::NS;
+                        const int b = g & 1;
+                        if (g >= 2) ok = mbar_wait_warp(bar(Bar::S_EMPTY + b), ((g - 2) >> 1) & 1, wc);
+                        ok = ok && mbar_wait_warp(bar(Bar::K_FULL + st), (g / C::NS) & 1, wc);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t k_tile = s_k + st * C::QK_BYTES;
+                        const uint32_t d_tmem = tmem + (b ? C::COL_S1 : C::COL_S0);
+                        if constexpr (FP8) {
+                            // E4M3 codes, 32 bytes of K per instruction, both
+                            // operands K-major in shared memory.
+                            constexpr uint32_t id_s8 = idesc_e4m3(128, 128);
+                            const uint32_t q_tile = s_q + (k & 1) * C::TILE_BYTES;
 #pragma unroll
-                                for (int kk = 0; kk < D / 32; ++kk) {
-                                    if constexpr (D == 128)
-                                        mma_ss_f8(d_tmem, smem_desc_sw128(q_tile + kk * 32, 16, 1024),
-                                                  smem_desc_sw128(k_tile + kk * 32, 16, 1024),
-                                                  id_s8, kk > 0);
-                                    else
-                                        mma_ss_f8(d_tmem, smem_desc_sw64(q_tile + kk * 32, 512),
-                                                  smem_desc_sw64(k_tile + kk * 32, 512), id_s8,
-                                                  kk > 0);
+                            for (int kk = 0; kk < D / 32; ++kk) {
+                                uint64_t ad, bd;
+                                if constexpr (D == 128) {
+                                    ad = smem_desc_sw128(q_tile + kk * 32, 16, 1024);
+                                    bd = smem_desc_sw128(k_tile + kk * 32, 16, 1024);
+                                } else {
+                                    ad = smem_desc_sw64(q_tile + kk * 32, 512);
+                                    bd = smem_desc_sw64(k_tile + kk * 32, 512);
                                 }
-                            } else {
-#pragma unroll
-                                for (int kk = 0; kk < D / 16; ++kk) {
-                                    const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                                    mma_ts(d_tmem, tmem + C::COL_Q + kk * 8,
-                                           smem_desc_sw128(k_tile + koff, 16, 1024), id_s, kk > 0);
-                                }
+                                if (elect_one()) mma_ss_f8(d_tmem, ad, bd, id_s8, kk > 0);
+                                __syncwarp();
                             }
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                                const uint64_t bd = smem_desc_sw128(k_tile + koff, 16, 1024);
+                                if (elect_one())
+                                    mma_ts(d_tmem, tmem + C::COL_Q + kk * 8, bd, id_s, kk > 0);
+                                __syncwarp();
+                            }
+                        }
+                        if (elect_one()) {
                             tc_commit(bar(Bar::S_FULL + b));
                             tc_commit(bar(Bar::K_EMPTY + st));
                         }
-                        // Q's TMEM columns are free once these MMAs have finished.
-                        if (!FP8 && ok) tc_commit(bar(Bar::QT_EMPTY));
+                        __syncwarp();
                     }
+                    // Q's TMEM columns are free once these MMAs have finished.
+                    if (!FP8 && ok && elect_one()) tc_commit(bar(Bar::QT_EMPTY));
+                    __syncwarp();
                 }
             }
-            __syncwarp();
         }
     } else {
         regs_increase<kRegsSoftmax>();
@@ -679,9 +700,10 @@ __global__ void __launch_bounds__(384, 1)
 
     // ---------------------------------------------------------------- teardown
     __syncthreads();
-    if (warp == 2 && lane == 0) tc_commit(bar(Bar::DONE));
+    // The commits come from the lane that issued each warp's MMAs.
+    if (warp == 2 && elect_one()) tc_commit(bar(Bar::DONE));
     if (warp == 1) {
-        if (lane == 0) {
+        if (elect_one()) {
             tc_commit(bar(Bar::DONE));  // both issuers' MMAs have completed
             mbar_wait_drain(bar(Bar::DONE), 0, timeout_ns);
         }

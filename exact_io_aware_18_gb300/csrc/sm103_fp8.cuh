@@ -32,11 +32,11 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint
 // aligned.  sbo is the byte stride between 8-row groups (512 for a dense
 // tile); the leading offset is not used.
 __device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t sbo_bytes) {
-    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
-           (static_cast<uint64_t>(1u) << 16) |                             // leading offset (unused)
-           (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) |
-           (1ull << 46) |  // descriptor version for tcgen05
-           (4ull << 61);   // 64-byte swizzle
+    const uint32_t lo = ((saddr & 0x3FFFFu) >> 4) | (1u << 16);  // leading offset (unused)
+    const uint32_t hi = ((sbo_bytes >> 4) & 0x3FFFu) |
+                        (1u << 14) |  // descriptor version for tcgen05 (bit 46)
+                        (4u << 29);   // 64-byte swizzle (bits 61-63)
+    return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 }  // namespace fa

@@ -88,6 +88,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+// mbar_wait by a whole converged warp; true only if every lane saw the phase
+// complete, so the warp stays converged whatever the outcome.  (Letting lane
+// 0 alone test the barrier and broadcasting its outcome measured more than
+// twice as slow in every kernel.)
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
+}
+
 // Bounded wait that ignores the abort flag.  Used only to drain copies and
 // MMAs that are already in flight before a CTA leaves, so that no
 // asynchronous unit still writes its shared or tensor memory afterwards.
@@ -272,6 +280,22 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
         : "memory");
 }
 
+// One lane of a converged warp, elected by elect.sync (with every lane active
+// it is the same lane each time, so the MMAs it issues and the commits that
+// track them come from one thread).  MMA issuers run as whole warps and issue
+// each tcgen05.mma and tcgen05.commit under this predicate: the descriptors
+// and TMEM addresses, computed by all lanes alike, can then stay
+// warp-uniform, and a chain of 128 x 128 x 16 MMAs with a barrier wait per
+// group of eight keeps the tensor pipe busy; the same chain issued by a lone
+// lane (an `if (lane == 0)` region) runs about 1.5 times slower.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // D(tmem) (+)= A(smem) * B(smem), kind::f16, one CTA.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -298,19 +322,24 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // between atoms along the leading / strided dimension; for K-major operands
 // whose K extent per instruction stays inside one 128-byte row the leading
 // offset is not used.
+// The two 32-bit words are built separately: the high word is a constant for
+// a given stride, and the low word costs one add per start address, which
+// keeps per-MMA descriptor arithmetic short on the issuing warp.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
                                                     uint32_t sbo_bytes) {
-    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
-           (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
-           (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) |
-           (1ull << 46) |  // descriptor version for tcgen05
-           (2ull << 61);   // 128-byte swizzle
+    const uint32_t lo = ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+    const uint32_t hi = ((sbo_bytes >> 4) & 0x3FFFu) |
+                        (1u << 14) |  // descriptor version for tcgen05 (bit 46)
+                        (2u << 29);   // 128-byte swizzle (bits 61-63)
+    return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 // Same descriptor with its start address moved by `bytes` (a multiple of
 // 16; the address field cannot overflow for shared-memory offsets < 256 KB).
+// Only the low word changes: one 32-bit add.
 __device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
-    return desc + (bytes >> 4);
+    const uint32_t lo = static_cast<uint32_t>(desc) + (bytes >> 4);
+    return (desc & 0xFFFFFFFF00000000ull) | lo;
 }
 
 // Instruction descriptor, kind::f16: BF16 A and B, FP32 accumulator, dense.

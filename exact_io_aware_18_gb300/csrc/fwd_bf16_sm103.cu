@@ -22,36 +22,35 @@
 //               shared-memory buffers.  It has a warp of its own: two lanes
 //               of one warp that both spin on barriers share one instruction
 //               stream, and the loads of one would wait on the other's spin.
-//   warps 1, 2  two MMA issuers (one thread each).  A: S_j = Q K_j^T into one
-//               of two TMEM score buffers, once the softmax warps have read
-//               S_{j-2} out of it.  B: O += P_j V_j as soon as the softmax
-//               warps release P_j.  Both take A from TMEM (Q, copied there
-//               once per tile, and P), so consecutive MMAs never switch the A
-//               source, which drains the tensor pipe.  One thread issues MMAs
-//               no faster than the pipe runs them, so two issuers keep it fed
-//               while either waits.
+//   warps 1, 2  two MMA issuers (whole warps; one elected lane issues).  A:
+//               S_j = Q K_j^T into one of two TMEM score buffers, once P V
+//               has read the probabilities of S_{j-2} out of it.  B: O +=
+//               P_j V_j as soon as the softmax warps release P_j.  Both take
+//               A from TMEM (Q, copied there once per tile, and P), so every
+//               MMA reads one operand tile from shared memory, not two.  Two
+//               issuers keep the pipe fed while either waits for its inputs.
 //   warps 4-11  softmax: thread (r, h) owns query row r (TMEM lane r) and
 //               keys [64h, 64h+64) of every tile (warps 4-7: h = 0, 8-11:
 //               h = 1), so two warps share each SM sub-partition's rows and
 //               hide each other's latency.  First, Q row half into TMEM.  Per
-//               tile: load its 64 scores (then the S buffer is free), mask,
-//               swap the partial row max with the partner warp through shared
-//               memory, update m and its half of l, write P as BF16 into the
-//               P buffer once PV_{j-1} has read it, and rescale its d/2
-//               columns of the O accumulator only when the max grew by more
-//               than 2^8 (the final O / l and LSE use the same stale max, so
-//               the result is unchanged).  After a Q tile's last key tile
-//               the next Q tile's Q goes into TMEM first, so that its first
-//               score MMAs run during this tile's epilogue: the two halves of
-//               l are summed, O / l goes to BF16 into the tile's Q buffer and
-//               out by TMA store; LSE = ln 2 * (m + log2 l).
+//               tile: load its 64 scores, mask, swap the partial row max with
+//               the partner warp through shared memory, update m and its half
+//               of l, write P as BF16 over the first half of its own score
+//               columns, and rescale its d/2 columns of the O accumulator
+//               (after PV_{j-1} has run) only when the max grew by more than
+//               2^8 (the final O / l and LSE use the same stale max, so the
+//               result is unchanged).  After a Q tile's last key tile the
+//               next Q tile's Q goes into TMEM first, so that its first score
+//               MMAs run during this tile's epilogue: the two halves of l are
+//               summed, O / l goes to BF16 into the tile's Q buffer and out by
+//               TMA store; LSE = ln 2 * (m + log2 l).
 // Warpgroup 0 (warps 0-3) hands registers to the softmax warpgroups, which
 // hold a row half of scores, probabilities and O in flight.
 //
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+d), Q [256+d, 256+3d/2),
-// P [256+3d/2, 320+3d/2) (all 512 columns at d = 128).  All waits are
-// bounded (see sm103_primitives.cuh); a CTA that gives up tells the others
-// through its abort flag and every role leaves at its next wait.
+// TMEM columns: S0 [0,128), S1 [128,256) (P_j as BF16 pairs at [0,32) and
+// [64,96) of its score buffer), O [256, 256+d), Q [256+d, 256+3d/2).  All
+// waits are bounded (see sm103_primitives.cuh); a CTA that gives up tells the
+// others through its abort flag and every role leaves at its next wait.
 #include "fa_internal.h"
 #include "sm103_fp8.cuh"
 #include "sm103_primitives.cuh"
@@ -93,8 +92,8 @@ struct FwdCfg {
     // S0, S1: scores (FP32); O: accumulator (FP32); Q and P: BF16 pairs, the
     // A operands of S = Q K^T and O += P V.
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
-    static constexpr uint32_t COL_Q = COL_O + D, COL_P = COL_Q + D / 2;
-    static_assert(COL_P + BN / 2 <= TMEM_COLS, "TMEM columns");
+    static constexpr uint32_t COL_Q = COL_O + D;
+    static_assert(COL_Q + D / 2 <= TMEM_COLS, "TMEM columns");
     static constexpr int THREADS = 384;
     // Arrivals on ITEM_EMPTY: the K/V producer, both issuers, 8 softmax warps.
     static constexpr int ITEM_READERS = 11;
@@ -113,9 +112,8 @@ struct FwdBars {
     static constexpr int S_EMPTY = S_FULL + 2;     // 2
     static constexpr int QT_FULL = S_EMPTY + 2;
     static constexpr int QT_EMPTY = QT_FULL + 1;
-    static constexpr int P_FULL = QT_EMPTY + 1;
-    static constexpr int O_FULL = P_FULL + 1;
-    static constexpr int ITEM_FULL = O_FULL + 1;   // QUEUE
+    static constexpr int P_FULL = QT_EMPTY + 1;    // 2
+    static constexpr int ITEM_FULL = P_FULL + 2;   // QUEUE
     static constexpr int ITEM_EMPTY = ITEM_FULL + QUEUE;
     static constexpr int CLAIM_OK = ITEM_EMPTY + QUEUE;
     static constexpr int DONE = CLAIM_OK + 1;
@@ -184,7 +182,8 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(bar(Bar::Q_FULL + b), 1);
             mbar_init(bar(Bar::Q_EMPTY + b), 1);
             mbar_init(bar(Bar::S_FULL + b), 1);
-            mbar_init(bar(Bar::S_EMPTY + b), 8);  // one arrival per softmax warp
+            mbar_init(bar(Bar::S_EMPTY + b), 1);  // P V of the buffer's P has run
+            mbar_init(bar(Bar::P_FULL + b), 8);   // one arrival per softmax warp
         }
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(bar(Bar::K_FULL + s), 1);
@@ -194,8 +193,6 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(bar(Bar::QT_FULL), 8);
         mbar_init(bar(Bar::QT_EMPTY), 1);
-        mbar_init(bar(Bar::P_FULL), 8);
-        mbar_init(bar(Bar::O_FULL), 1);
         for (int i = 0; i < C::QUEUE; ++i) {
             mbar_init(bar(Bar::ITEM_FULL + i), 1);
             mbar_init(bar(Bar::ITEM_EMPTY + i), C::ITEM_READERS);
@@ -362,30 +359,34 @@ __global__ void __launch_bounds__(384, 1)
                     // Issuer B: O += P_j V_j as soon as the softmax warps release P_j.
                     for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
                         const int st = g % C::NS;
-                        ok = mbar_wait_warp(bar(Bar::P_FULL), g & 1, wc) &&
+                        const int b = g & 1;
+                        ok = mbar_wait_warp(bar(Bar::P_FULL + b), (g >> 1) & 1, wc) &&
                              mbar_wait_warp(bar(Bar::V_FULL + st), (g / C::NS) & 1, wc);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t v_tile = s_v + st * C::TILE_BYTES;
+                        // P_j (BF16) over its own scores: keys [64h, 64h+64) at
+                        // columns [64h, 64h+32) of S buffer b.
+                        const uint32_t p_cols = tmem + (b ? C::COL_S1 : C::COL_S0);
 #pragma unroll
                         for (int kk = 0; kk < C::BN / 16; ++kk) {
                             // V as an MN-major B operand: 16 keys = 2 atoms of 8 rows.
                             const uint64_t bd =
                                 smem_desc_sw128(v_tile + kk * 2048, C::BOX_BYTES, 1024);
                             if (elect_one())
-                                mma_ts(tmem + C::COL_O, tmem + C::COL_P + kk * 8, bd, id_pv,
-                                       (j > w.j0 || kk > 0));
+                                mma_ts(tmem + C::COL_O, p_cols + (kk >> 2) * 64 + (kk & 3) * 8, bd,
+                                       id_pv, (j > w.j0 || kk > 0));
                             __syncwarp();
                         }
                         if (elect_one()) {
                             tc_commit(bar(Bar::V_EMPTY + st));
-                            tc_commit(bar(Bar::O_FULL));
+                            tc_commit(bar(Bar::S_EMPTY + b));  // P_j read: S buffer b is free
                         }
                         __syncwarp();
                     }
                 } else {
-                    // Issuer A: S_j = Q K_j^T into buffer g & 1 once the softmax
-                    // warps have read S_{g-2} out of it (the next phase of that
+                    // Issuer A: S_j = Q K_j^T into buffer g & 1 once P V_{g-2}
+                    // has read P_{g-2} out of it (the next phase of that
                     // S_EMPTY needs S_g itself, so the wait cannot miss it).
                     // Q in TMEM (BF16) or Q's E4M3 tile in shared memory (FP8).
                     if constexpr (FP8) ok = mbar_wait_warp(bar(Bar::Q_FULL + (k & 1)), (k >> 1) & 1, wc);
@@ -540,10 +541,6 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
                     }
-                    // S is in registers: its buffer may take the tile after next.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(Bar::S_EMPTY + b));
                     const int key0 = j * C::BN + 64 * h;  // key index of entry 0
                     if ((CAUSAL && j == qt) || key0 + 64 > Nk) {
 #pragma unroll
@@ -578,16 +575,19 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 const float sum = sum2.x + sum2.y;
                 l_run = l_run * alpha + sum;
-                if (j > w.j0) {
-                    // PV_{j-1} has finished: the P buffer is free, and O holds
-                    // the sum up to PV_{j-1}, as a rescale needs.
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::O_FULL), (g - 1) & 1, wc));
+                const bool any_rescale = __any_sync(0xffffffffu, rescale) && j > w.j0;
+                if (any_rescale) {
+                    // A rescale of O needs PV_{j-1} to have run (O then holds
+                    // the sum up to it): its commit frees the other S buffer.
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_EMPTY + (b ^ 1)),
+                                                           ((g - 1) >> 1) & 1, wc));
                     if (!ok) continue;  // the next pair barrier (or the loop end) reports it
                     tc_fence_after();
                 }
-                // P (BF16): keys [64h, 64h+64) at P columns [32h, 32h+32).
-                tmem_st32(t_lane + C::COL_P + 32 * h, pk);
-                if (__any_sync(0xffffffffu, rescale) && j > w.j0) {
+                // P (BF16) over this thread's scores, already in registers:
+                // keys [64h, 64h+64) at columns [64h, 64h+32) of S buffer b.
+                tmem_st32(t_s, pk);
+                if (any_rescale) {
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c) {
                         uint32_t r[32];
@@ -607,7 +607,7 @@ __global__ void __launch_bounds__(384, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(Bar::P_FULL));
+                if (lane == 0) mbar_arrive(bar(Bar::P_FULL + b));
                 if (j == w.j0 && threadIdx.x == kStoreThread && pending_qb >= 0) {
                     // The previous tile's O store has had a whole tile of time:
                     // wait for it to finish reading its Q buffer, then free it.
@@ -625,7 +625,9 @@ __global__ void __launch_bounds__(384, 1)
             xch[512 + h * 128 + row] = l_run;
             ok = named_bar_and(pair_bar, 64, ok);
             const float l_tot = l_run + xch[512 + (h ^ 1) * 128 + row];
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::O_FULL), (g - 1) & 1, wc));
+            if (ok)  // the tile's last P V has run
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_EMPTY + ((g - 1) & 1)),
+                                                       ((g - 1) >> 1) & 1, wc));
             if (ok) {
                 tc_fence_after();
                 const float inv_l = 1.f / l_tot;

@@ -16,41 +16,40 @@
 // a time so that their K/V tiles stay in L2).  Tiles run back to back: the
 // next tile's Q is loaded and its first scores computed while the current
 // one finishes, and its O store drains while the next one runs.
-//   warp 0      loads K_j and V_j into an NS-deep ring (128-byte swizzle,
-//               64-column boxes).
+//   warp 0      loads K_j and V_j into NS-deep rings (128-byte swizzle,
+//               64-column boxes), K one key tile ahead of V.
 //   warp 3      claims tiles and loads each Q tile into one of two
 //               shared-memory buffers.  It has a warp of its own: two lanes
 //               of one warp that both spin on barriers share one instruction
 //               stream, and the loads of one would wait on the other's spin.
 //   warps 1, 2  two MMA issuers (whole warps; one elected lane issues).  A:
-//               S_j = Q K_j^T into one of two TMEM score buffers, once P V
-//               has read the probabilities of S_{j-2} out of it.  B: O +=
-//               P_j V_j as soon as the softmax warps release P_j.  Both take
-//               A from TMEM (Q, copied there once per tile, and P), so every
-//               MMA reads one operand tile from shared memory, not two.  Two
-//               issuers keep the pipe fed while either waits for its inputs.
+//               S_j = Q K_j^T (both operands in shared memory) into one of
+//               three TMEM score buffers, once P V has read the probabilities
+//               of S_{j-3} out of it.  B: O += P_j V_j (P from TMEM) as soon as
+//               the softmax warps release P_j.  Three score buffers let S_{j+1}
+//               run while P V_{j-1} and the softmax of tile j are in flight.
 //   warps 4-11  softmax: thread (r, h) owns query row r (TMEM lane r) and
 //               keys [64h, 64h+64) of every tile (warps 4-7: h = 0, 8-11:
 //               h = 1), so two warps share each SM sub-partition's rows and
-//               hide each other's latency.  First, Q row half into TMEM.  Per
-//               tile: load its 64 scores, mask, swap the partial row max with
-//               the partner warp through shared memory, update m and its half
-//               of l, write P as BF16 over the first half of its own score
-//               columns, and rescale its d/2 columns of the O accumulator
-//               (after PV_{j-1} has run) only when the max grew by more than
-//               2^8 (the final O / l and LSE use the same stale max, so the
-//               result is unchanged).  After a Q tile's last key tile the
-//               next Q tile's Q goes into TMEM first, so that its first score
+//               hide each other's latency.  Per tile: load its 64 scores, mask,
+//               swap the partial row max with the partner warp through shared
+//               memory, update m and its half of l, write P as BF16 over the
+//               first half of its own score columns, and rescale its d/2
+//               columns of the O accumulator (after PV_{j-1} has run) only when
+//               the max grew by more than 2^8 (the final O / l and LSE use the
+//               same stale max, so the result is unchanged).  After a Q tile's
+//               last key tile the next tile is taken, so that its first score
 //               MMAs run during this tile's epilogue: the two halves of l are
-//               summed, O / l goes to BF16 into the tile's Q buffer and out by
-//               TMA store; LSE = ln 2 * (m + log2 l).
+//               summed, O / l goes to BF16 into the tile's Q buffer (its score
+//               MMAs are done) and out by TMA store; LSE = ln 2 * (m + log2 l).
 // Warpgroup 0 (warps 0-3) hands registers to the softmax warpgroups, which
 // hold a row half of scores, probabilities and O in flight.
 //
-// TMEM columns: S0 [0,128), S1 [128,256) (P_j as BF16 pairs at [0,32) and
-// [64,96) of its score buffer), O [256, 256+d), Q [256+d, 256+3d/2).  All
-// waits are bounded (see sm103_primitives.cuh); a CTA that gives up tells the
-// others through its abort flag and every role leaves at its next wait.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+d), S2 [256+d,
+// 384+d); tile j's P as BF16 pairs at [0,32) and [64,96) of its score
+// buffer.  All waits are bounded (see sm103_primitives.cuh); a CTA that gives
+// up tells the others through its abort flag and every role leaves at its
+// next wait.
 #include "fa_internal.h"
 #include "sm103_fp8.cuh"
 #include "sm103_primitives.cuh"
@@ -89,11 +88,15 @@ struct FwdCfg {
     static constexpr int SMEM_BYTES = LAYOUT_BYTES + 1024;  // + alignment slack
     static_assert(SMEM_BYTES <= kMaxDynSmem, "forward tiles do not fit in shared memory");
     static constexpr uint32_t TMEM_COLS = 512;
-    // S0, S1: scores (FP32); O: accumulator (FP32); Q and P: BF16 pairs, the
-    // A operands of S = Q K^T and O += P V.
-    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
-    static constexpr uint32_t COL_Q = COL_O + D;
-    static_assert(COL_Q + D / 2 <= TMEM_COLS, "TMEM columns");
+    // Three FP32 score buffers (S0, S1 around the O accumulator, S2 after
+    // it); the BF16 P of each tile is written over the first half of its own
+    // scores.  Q stays in shared memory.
+    static constexpr int NSB = 3;
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_S2 = COL_O + D;
+    static_assert(COL_S2 + BN <= TMEM_COLS, "TMEM columns");
+    __device__ static constexpr uint32_t col_s(int b) {
+        return b == 0 ? COL_S0 : (b == 1 ? COL_S1 : COL_S2);
+    }
     static constexpr int THREADS = 384;
     // Arrivals on ITEM_EMPTY: the K/V producer, both issuers, 8 softmax warps.
     static constexpr int ITEM_READERS = 11;
@@ -108,12 +111,11 @@ struct FwdBars {
     static constexpr int V_FULL = K_FULL + NS;
     static constexpr int K_EMPTY = V_FULL + NS;
     static constexpr int V_EMPTY = K_EMPTY + NS;
-    static constexpr int S_FULL = V_EMPTY + NS;    // 2
-    static constexpr int S_EMPTY = S_FULL + 2;     // 2
-    static constexpr int QT_FULL = S_EMPTY + 2;
-    static constexpr int QT_EMPTY = QT_FULL + 1;
-    static constexpr int P_FULL = QT_EMPTY + 1;    // 2
-    static constexpr int ITEM_FULL = P_FULL + 2;   // QUEUE
+    // One S_FULL / S_EMPTY / P_FULL triple per score buffer.
+    static constexpr int S_FULL = V_EMPTY + NS;    // 3
+    static constexpr int S_EMPTY = S_FULL + 3;     // 3
+    static constexpr int P_FULL = S_EMPTY + 3;     // 3
+    static constexpr int ITEM_FULL = P_FULL + 3;   // QUEUE
     static constexpr int ITEM_EMPTY = ITEM_FULL + QUEUE;
     static constexpr int CLAIM_OK = ITEM_EMPTY + QUEUE;
     static constexpr int DONE = CLAIM_OK + 1;
@@ -181,6 +183,8 @@ __global__ void __launch_bounds__(384, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(Bar::Q_FULL + b), 1);
             mbar_init(bar(Bar::Q_EMPTY + b), 1);
+        }
+        for (int b = 0; b < C::NSB; ++b) {
             mbar_init(bar(Bar::S_FULL + b), 1);
             mbar_init(bar(Bar::S_EMPTY + b), 1);  // P V of the buffer's P has run
             mbar_init(bar(Bar::P_FULL + b), 8);   // one arrival per softmax warp
@@ -191,8 +195,6 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(bar(Bar::K_EMPTY + s), 1);
             mbar_init(bar(Bar::V_EMPTY + s), 1);
         }
-        mbar_init(bar(Bar::QT_FULL), 8);
-        mbar_init(bar(Bar::QT_EMPTY), 1);
         for (int i = 0; i < C::QUEUE; ++i) {
             mbar_init(bar(Bar::ITEM_FULL + i), 1);
             mbar_init(bar(Bar::ITEM_EMPTY + i), C::ITEM_READERS);
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(384, 1)
         if (warp == 3) {
             if (lane == 0) {
                 // ------------------------------------------------ scheduler + Q loads
-                // Tile k+1 is claimed once the K/V loads of tile k have all been
+                // Tile k+1 is claimed once the K loads of tile k have all been
                 // issued (a few key tiles before its end: early enough to hide the
                 // Q load, late enough that the CTAs that finish first get the
                 // remaining work), its Q buffer is free (the store of tile k-1 has
@@ -304,38 +306,72 @@ __global__ void __launch_bounds__(384, 1)
         } else if (warp == 0) {
             if (lane == 0) {
                 // ------------------------------------------------ K/V producer
-                int g = 0, k_issued = 0, v_issued = 0;
+                // K runs one key tile ahead of V over the stream of key tiles
+                // of consecutive Q tiles: the next score MMAs need K_{g+1}
+                // while P V_g still waits for V_g, and a K stage frees (after
+                // its S) earlier than a V stage (after its P V).
+                int k_issued = 0, v_issued = 0;
                 bool ok = true;
-                for (int k = 0; ok; ++k) {
-                    const int item = take_item(k);
-                    if (item < 0) break;
-                    const Work w = work_of(item);
-                    // K/V head of query head w.bh: its group's head.
-                    const int bkv = (w.bh / Hq) * (Hq / n_rep) + (w.bh % Hq) / n_rep;
-                    for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
-                        const int st = g % C::NS;
-                        const int use = g / C::NS;
-                        if (use > 0) ok = mbar_wait(bar(Bar::K_EMPTY + st), (use - 1) & 1, wc);
-                        if (!ok) break;
-                        mbar_arrive_expect_tx(bar(Bar::K_FULL + st), C::QK_BYTES);
-                        if constexpr (FP8) {
-                            tma_load_3d(s_k + st * C::QK_BYTES, &tm_k, bar(Bar::K_FULL + st), 0,
-                                        j * C::BN, bkv);
-                        } else {
-                            for (int kb = 0; kb < C::KB; ++kb)
-                                tma_load_3d(s_k + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_k,
-                                            bar(Bar::K_FULL + st), kb * 64, j * C::BN, bkv);
-                        }
-                        k_issued = g + 1;
-                        if (use > 0) ok = mbar_wait(bar(Bar::V_EMPTY + st), (use - 1) & 1, wc);
-                        if (!ok) break;
-                        mbar_arrive_expect_tx(bar(Bar::V_FULL + st), C::TILE_BYTES);
+                auto head_of = [&](int bh) { return (bh / Hq) * (Hq / n_rep) + (bh % Hq) / n_rep; };
+                auto issue_k = [&](int j, int bkv) -> bool {
+                    const int g = k_issued, st = g % C::NS, use = g / C::NS;
+                    if (use > 0 && !mbar_wait(bar(Bar::K_EMPTY + st), (use - 1) & 1, wc)) return false;
+                    mbar_arrive_expect_tx(bar(Bar::K_FULL + st), C::QK_BYTES);
+                    if constexpr (FP8) {
+                        tma_load_3d(s_k + st * C::QK_BYTES, &tm_k, bar(Bar::K_FULL + st), 0,
+                                    j * C::BN, bkv);
+                    } else {
                         for (int kb = 0; kb < C::KB; ++kb)
-                            tma_load_3d(s_v + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_v,
-                                        bar(Bar::V_FULL + st), kb * 64, j * C::BN, bkv);
-                        v_issued = g + 1;
+                            tma_load_3d(s_k + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_k,
+                                        bar(Bar::K_FULL + st), kb * 64, j * C::BN, bkv);
                     }
-                    if (ok) mbar_arrive(bar(Bar::CLAIM_OK));  // the next tile may be claimed
+                    k_issued = g + 1;
+                    return true;
+                };
+                auto issue_v = [&](int j, int bkv) -> bool {
+                    const int g = v_issued, st = g % C::NS, use = g / C::NS;
+                    if (use > 0 && !mbar_wait(bar(Bar::V_EMPTY + st), (use - 1) & 1, wc)) return false;
+                    mbar_arrive_expect_tx(bar(Bar::V_FULL + st), C::TILE_BYTES);
+                    for (int kb = 0; kb < C::KB; ++kb)
+                        tma_load_3d(s_v + st * C::TILE_BYTES + kb * C::BOX_BYTES, &tm_v,
+                                    bar(Bar::V_FULL + st), kb * 64, j * C::BN, bkv);
+                    v_issued = g + 1;
+                    return true;
+                };
+                // The K cursor: Q tile ck, key tile cj of it, K/V head cbkv.
+                int ck = 0, cj = 0, cbkv = 0;
+                Work cw{};
+                // Moves the cursor to the next key tile, taking Q tiles from
+                // the queue as it leaves one (and letting the next be claimed:
+                // every K load of the tile left behind has been issued); false
+                // at the end of the work.
+                auto advance = [&]() -> bool {
+                    ++cj;
+                    while (cj >= cw.j1) {
+                        mbar_arrive(bar(Bar::CLAIM_OK));
+                        const int nitem = take_item(ck + 1);
+                        if (nitem < 0) return false;
+                        ++ck;
+                        cw = work_of(nitem);
+                        cj = cw.j0;
+                        cbkv = head_of(cw.bh);
+                    }
+                    return true;
+                };
+                const int item0 = take_item(0);
+                bool more = false;
+                if (item0 >= 0) {
+                    cw = work_of(item0);
+                    cj = cw.j0 - 1;
+                    cbkv = head_of(cw.bh);
+                    more = advance();
+                }
+                if (more) ok = issue_k(cj, cbkv);
+                while (more && ok) {
+                    const int vj = cj, vbkv = cbkv;
+                    more = advance();
+                    if (more) ok = issue_k(cj, cbkv);
+                    ok = ok && issue_v(vj, vbkv);
                 }
                 for (int t = (k_issued > C::NS ? k_issued - C::NS : 0); t < k_issued; ++t)
                     mbar_wait_drain(bar(Bar::K_FULL + t % C::NS), (t / C::NS) & 1, timeout_ns);
@@ -359,15 +395,15 @@ __global__ void __launch_bounds__(384, 1)
                     // Issuer B: O += P_j V_j as soon as the softmax warps release P_j.
                     for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
                         const int st = g % C::NS;
-                        const int b = g & 1;
-                        ok = mbar_wait_warp(bar(Bar::P_FULL + b), (g >> 1) & 1, wc) &&
+                        const int b = g % C::NSB;
+                        ok = mbar_wait_warp(bar(Bar::P_FULL + b), (g / C::NSB) & 1, wc) &&
                              mbar_wait_warp(bar(Bar::V_FULL + st), (g / C::NS) & 1, wc);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t v_tile = s_v + st * C::TILE_BYTES;
                         // P_j (BF16) over its own scores: keys [64h, 64h+64) at
                         // columns [64h, 64h+32) of S buffer b.
-                        const uint32_t p_cols = tmem + (b ? C::COL_S1 : C::COL_S0);
+                        const uint32_t p_cols = tmem + C::col_s(b);
 #pragma unroll
                         for (int kk = 0; kk < C::BN / 16; ++kk) {
                             // V as an MN-major B operand: 16 keys = 2 atoms of 8 rows.
@@ -385,26 +421,26 @@ __global__ void __launch_bounds__(384, 1)
                         __syncwarp();
                     }
                 } else {
-                    // Issuer A: S_j = Q K_j^T into buffer g & 1 once P V_{g-2}
-                    // has read P_{g-2} out of it (the next phase of that
+                    // Issuer A: S_j = Q K_j^T into buffer g % 3 once P V_{g-3}
+                    // has read P_{g-3} out of it (the next phase of that
                     // S_EMPTY needs S_g itself, so the wait cannot miss it).
-                    // Q in TMEM (BF16) or Q's E4M3 tile in shared memory (FP8).
-                    if constexpr (FP8) ok = mbar_wait_warp(bar(Bar::Q_FULL + (k & 1)), (k >> 1) & 1, wc);
-                    else ok = mbar_wait_warp(bar(Bar::QT_FULL), k & 1, wc);
+                    // Q (BF16 tile or E4M3 codes) in shared memory, buffer k & 1.
+                    ok = mbar_wait_warp(bar(Bar::Q_FULL + (k & 1)), (k >> 1) & 1, wc);
+                    const uint32_t q_tile = s_q + (k & 1) * C::TILE_BYTES;
                     for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
                         const int st = g % C::NS;
-                        const int b = g & 1;
-                        if (g >= 2) ok = mbar_wait_warp(bar(Bar::S_EMPTY + b), ((g - 2) >> 1) & 1, wc);
+                        const int b = g % C::NSB;
+                        if (g >= C::NSB)
+                            ok = mbar_wait_warp(bar(Bar::S_EMPTY + b), ((g - C::NSB) / C::NSB) & 1, wc);
                         ok = ok && mbar_wait_warp(bar(Bar::K_FULL + st), (g / C::NS) & 1, wc);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t k_tile = s_k + st * C::QK_BYTES;
-                        const uint32_t d_tmem = tmem + (b ? C::COL_S1 : C::COL_S0);
+                        const uint32_t d_tmem = tmem + C::col_s(b);
                         if constexpr (FP8) {
                             // E4M3 codes, 32 bytes of K per instruction, both
                             // operands K-major in shared memory.
                             constexpr uint32_t id_s8 = idesc_e4m3(128, 128);
-                            const uint32_t q_tile = s_q + (k & 1) * C::TILE_BYTES;
 #pragma unroll
                             for (int kk = 0; kk < D / 32; ++kk) {
                                 uint64_t ad, bd;
@@ -422,9 +458,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk) {
                                 const uint32_t koff = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                                const uint64_t ad = smem_desc_sw128(q_tile + koff, 16, 1024);
                                 const uint64_t bd = smem_desc_sw128(k_tile + koff, 16, 1024);
-                                if (elect_one())
-                                    mma_ts(d_tmem, tmem + C::COL_Q + kk * 8, bd, id_s, kk > 0);
+                                if (elect_one()) mma_ss(d_tmem, ad, bd, id_s, kk > 0);
                                 __syncwarp();
                             }
                         }
@@ -434,9 +470,6 @@ __global__ void __launch_bounds__(384, 1)
                         }
                         __syncwarp();
                     }
-                    // Q's TMEM columns are free once these MMAs have finished.
-                    if (!FP8 && ok && elect_one()) tc_commit(bar(Bar::QT_EMPTY));
-                    __syncwarp();
                 }
             }
         }
@@ -465,42 +498,8 @@ __global__ void __launch_bounds__(384, 1)
             if (okq && lane == 0) mbar_arrive(bar(Bar::ITEM_EMPTY + slot));
             return named_bar_and(5, 256, okq && item >= 0) ? item : -1;
         };
-        // Q of tile k into TMEM as BF16 pairs (the A operand of S = Q K^T):
-        // this thread's row, elements [h d/2, (h+1) d/2), read from the
-        // swizzled tile, once the previous tile's S MMAs have finished with it.
-        // (FP8: the S MMAs read Q's codes from shared memory; nothing to copy.)
-        auto copy_q = [&](int k) -> bool {
-            if constexpr (FP8) return true;
-            const int qb = k & 1;
-            const bool ok = __all_sync(
-                0xffffffffu, mbar_wait(bar(Bar::Q_FULL + qb), (k >> 1) & 1, wc) &&
-                                 (k == 0 || mbar_wait(bar(Bar::QT_EMPTY), (k - 1) & 1, wc)));
-            if (ok) {
-                tc_fence_after();
-                const uint32_t q_buf = C::OFF_Q + qb * C::TILE_BYTES;
-                uint32_t qw[D / 4];
-#pragma unroll
-                for (int c = 0; c < D / 16; ++c) {
-                    const int gc = h * (D / 16) + c;  // 16-byte chunk of the row
-                    const uint4 v = *reinterpret_cast<const uint4*>(
-                        smem + q_buf + (gc >> 3) * C::BOX_BYTES + row * 128 +
-                        (((gc & 7) ^ (row & 7)) << 4));
-                    qw[4 * c] = v.x;
-                    qw[4 * c + 1] = v.y;
-                    qw[4 * c + 2] = v.z;
-                    qw[4 * c + 3] = v.w;
-                }
-                if constexpr (D == 128) tmem_st32(t_lane + C::COL_Q + h * (D / 4), qw);
-                else tmem_st16(t_lane + C::COL_Q + h * (D / 4), qw);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(Bar::QT_FULL));
-            }
-            return ok;
-        };
         int item = take(0);
-        bool q_ok = item >= 0 && copy_q(0);
+        bool q_ok = item >= 0;
         for (int k = 0; item >= 0; ++k) {
             const Work w = work_of(item);
             const int qt = w.qt;
@@ -518,18 +517,18 @@ __global__ void __launch_bounds__(384, 1)
                                   : scale_log2;
             const int bkv = (bh / Hq) * (Hq / n_rep) + (bh % Hq) / n_rep;
             for (int j = w.j0; j < w.j1; ++j, ++g) {
-                const int b = g & 1;
+                const int b = g % C::NSB;
                 // Factor from S to base-2 exponents for this key tile (at
                 // least FLT_MIN, so that masked entries stay -inf).
                 const float c_s =
                     FP8 ? fmaxf(c_q * k_scale[static_cast<long long>(bkv) * n_kv_tiles + j],
                                 1.17549435e-38f)
                         : scale_log2;
-                const uint32_t t_s = t_lane + (b ? C::COL_S1 : C::COL_S0) + 64 * h;
+                const uint32_t t_s = t_lane + C::col_s(b) + 64 * h;
                 // A failed wait is carried to the pair barrier rather than
                 // breaking here, so that both warps leave the loop together.
                 const bool okw = ok && __all_sync(0xffffffffu,
-                                                  mbar_wait(bar(Bar::S_FULL + b), (g >> 1) & 1, wc));
+                                                  mbar_wait(bar(Bar::S_FULL + b), (g / C::NSB) & 1, wc));
                 float s[64];
                 float mx = -INFINITY;
                 if (okw) {
@@ -552,10 +551,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                     for (int c = 0; c < 64; c += 2) mx = fmax3(mx, s[c], s[c + 1]);
                 }
-                xch[(b * 2 + h) * 128 + row] = mx;
+                xch[((g & 1) * 2 + h) * 128 + row] = mx;
                 ok = named_bar_and(pair_bar, 64, okw);
                 if (!ok) break;
-                const float m_tile = fmaxf(mx, xch[(b * 2 + (h ^ 1)) * 128 + row]) * c_s;
+                const float m_tile = fmaxf(mx, xch[((g & 1) * 2 + (h ^ 1)) * 128 + row]) * c_s;
                 const bool rescale = m_tile > m_run + 8.0f;
                 float alpha = 1.f;
                 if (rescale) {
@@ -578,9 +577,9 @@ __global__ void __launch_bounds__(384, 1)
                 const bool any_rescale = __any_sync(0xffffffffu, rescale) && j > w.j0;
                 if (any_rescale) {
                     // A rescale of O needs PV_{j-1} to have run (O then holds
-                    // the sum up to it): its commit frees the other S buffer.
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_EMPTY + (b ^ 1)),
-                                                           ((g - 1) >> 1) & 1, wc));
+                    // the sum up to it): its commit frees the previous S buffer.
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_EMPTY + (g - 1) % C::NSB),
+                                                           ((g - 1) / C::NSB) & 1, wc));
                     if (!ok) continue;  // the next pair barrier (or the loop end) reports it
                     tc_fence_after();
                 }
@@ -616,18 +615,17 @@ __global__ void __launch_bounds__(384, 1)
                     pending_qb = -1;
                 }
             }
-            // The next tile's Q goes into TMEM now, before this tile's
-            // epilogue, so that its first score MMAs run meanwhile (its S
-            // buffers are free, and its first P V waits for its own P).
+            // The next tile is taken before this tile's epilogue; its first
+            // score MMAs (Q from shared memory) run meanwhile.
             const int next = take(k + 1);
-            q_ok = next >= 0 && copy_q(k + 1);
+            q_ok = next >= 0;
             // Both warps of the pair reach this barrier after the same iteration.
             xch[512 + h * 128 + row] = l_run;
             ok = named_bar_and(pair_bar, 64, ok);
             const float l_tot = l_run + xch[512 + (h ^ 1) * 128 + row];
             if (ok)  // the tile's last P V has run
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_EMPTY + ((g - 1) & 1)),
-                                                       ((g - 1) >> 1) & 1, wc));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::S_EMPTY + (g - 1) % C::NSB),
+                                                       ((g - 1) / C::NSB) & 1, wc));
             if (ok) {
                 tc_fence_after();
                 const float inv_l = 1.f / l_tot;
@@ -654,7 +652,7 @@ __global__ void __launch_bounds__(384, 1)
                     }
                 } else {
                     if (h == 0 && grow < N) lse[static_cast<long long>(bh) * N + grow] = lse_row;
-                    // O / l -> bf16 into this tile's Q buffer (Q is in TMEM now),
+                    // O / l -> bf16 into this tile's Q buffer (its score MMAs are done),
                     // in the TMA box layout: this half's d/2 columns are
                     // 32-column chunks h d/64 ... .
                     uint8_t* stage = smem + q_buf;

@@ -548,8 +548,14 @@ __global__ void __launch_bounds__(384, 1)
                             if ((CAUSAL && key > grow) || key >= Nk) s[c] = -INFINITY;
                         }
                     }
+                    // Four independent running maxima, then their max: a chain
+                    // of 8 three-input max instructions instead of 32.
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int c = 0; c < 64; c += 2) mx = fmax3(mx, s[c], s[c + 1]);
+                    for (int c = 0; c < 64; c += 8)
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + 2 * u], s[c + 2 * u + 1]);
+                    mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
                 }
                 xch[((g & 1) * 2 + h) * 128 + row] = mx;
                 ok = named_bar_and(pair_bar, 64, okw);

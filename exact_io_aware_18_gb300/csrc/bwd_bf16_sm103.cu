@@ -26,10 +26,8 @@
 //               stage, then V_j once issuer B's last dP^T has; per Q tile, a
 //               two-deep ring of [Q_i | dO_i] stages plus the 128-entry LSE2 /
 //               D vectors.
-//   warps 1, 2  two MMA issuers (one thread each).  A single thread issues a
-//               128 x 128 x 16 tcgen05.mma about as fast as the tensor pipe
-//               runs it, so with two issuers one keeps the pipe fed while the
-//               other waits.  Each issuer overwrites only TMEM it alone reads,
+//   warps 1, 2  two MMA issuers (whole warps; one elected lane issues), so
+//               that one keeps the pipe fed while the other waits.  Each issuer overwrites only TMEM it alone reads,
 //               after those reads in its own issue order:
 //                 issuer A: dV += P^T_t dO_t (A = P^T in TMEM, after P_FULL),
 //                           then S^T_t+1 = K Q_t+1^T over P^T_t;
@@ -45,7 +43,9 @@
 //               (warps 4-7: h = 0, warps 8-11: h = 1).  Phase P: 64 entries of
 //               the P^T row = exp2(S^T * scale*log2e - LSE2), kept in
 //               registers and written back as BF16 into the first 32 of its
-//               own 64 S^T columns.  Phase dS: dS^T = P o (dP^T - D), BF16,
+//               own 64 S^T columns, in two parts of 32 entries, each released
+//               to issuer A on its own barrier, so that dV's products for the
+//               first part run while the second is computed.  Phase dS: dS^T = P o (dP^T - D), BF16,
 //               likewise into its own dP^T columns (scale is applied to dK
 //               once, when it leaves TMEM).
 //   warps 12-15 epilogue: warp w reads rows 32 (w % 4) .. +32 of dV, then of
@@ -112,8 +112,12 @@ struct BwdBars {
     static constexpr int Q_EMPTY = Q_FULL + NSQ;
     static constexpr int S_FULL = Q_EMPTY + NSQ;
     static constexpr int DP_FULL = S_FULL + 1;
+    // P^T is released in two parts (queries 0-31 and 64-95, then 32-63 and
+    // 96-127), so that dV's first four products start while the second part
+    // is computed.
     static constexpr int P_FULL = DP_FULL + 1;
-    static constexpr int DS_FULL = P_FULL + 1;
+    static constexpr int P_FULL2 = P_FULL + 1;
+    static constexpr int DS_FULL = P_FULL2 + 1;
     static constexpr int ACC_FULL = DS_FULL + 1;
     static constexpr int DV_FREE = ACC_FULL + 1;
     static constexpr int DK_FREE = DV_FREE + 1;
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(bar(Bar::S_FULL), 1);
         mbar_init(bar(Bar::DP_FULL), 1);
         mbar_init(bar(Bar::P_FULL), C::COMPUTE_WARPS);
+        mbar_init(bar(Bar::P_FULL2), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::DS_FULL), C::COMPUTE_WARPS);
         mbar_init(bar(Bar::ACC_FULL), 2);
         mbar_init(bar(Bar::DV_FREE), 4);  // one arrival per epilogue warp
@@ -414,15 +419,28 @@ __global__ void __launch_bounds__(512, 1)
                         // P^T / dS^T (queries 0-63, 64-127) sit at columns [0,32)
                         // and [64,96) of their fp32 region.
                         const uint64_t d_mn = desc_advance(d_mn0, st * C::STAGE_BYTES);
+                        // Queries 0-31 and 64-95 first (products 0, 1, 4, 5), then
+                        // 32-63 and 96-127; issuer A waits for the second part of
+                        // P^T in between.
 #pragma unroll
-                        for (int kk = 0; kk < C::BM / 16; ++kk) {
-                            const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-                            const uint64_t bd = desc_advance(d_mn, kk * 2048);
-                            if (elect_one())
-                                mma_ts(tmem + c_acc, tmem + c_a + acol, bd, id_kv,
-                                       (t > 0 || kk > 0) ? 1u : 0u);
-                            __syncwarp();
+                        for (int part = 0; part < 2; ++part) {
+                            if (part == 1 && issuer_a) {
+                                ok = mbar_wait_warp(bar(Bar::P_FULL2), g & 1, wc);
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int kk = (u < 2 ? u : u + 2) + 2 * part;
+                                const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                                const uint64_t bd = desc_advance(d_mn, kk * 2048);
+                                if (elect_one())
+                                    mma_ts(tmem + c_acc, tmem + c_a + acol, bd, id_kv,
+                                           (t > 0 || kk > 0) ? 1u : 0u);
+                                __syncwarp();
+                            }
                         }
+                        if (!ok) break;
                         // This issuer no longer reads stage g.
                         if (elect_one()) tc_commit(bar(Bar::Q_EMPTY + st));
                         __syncwarp();
@@ -503,44 +521,46 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_after();
                 const float* l2v = vec_base + st * 256 + 64 * h;
                 const float* dlt = vec_base + st * 256 + 128 + 64 * h;
-                // Phase P: entries [64h, 64h+64) of this key's row of P^T.
+                // Phase P: entries [64h, 64h+64) of this key's row of P^T, in
+                // two parts of 32; part q's BF16 pairs go over score columns
+                // [64h + 16q, 64h + 16q + 16), already loaded.
                 float p[64];
-                {
-                    uint32_t sr[64];
-                    tmem_ld64(t_lane + C::COL_S + 64 * h, sr);
-                    const int q0 = i * C::BM + 64 * h;  // query index of entry 0
-                    const float2 c2 = make_float2(scale_log2, scale_log2);
-                    const float4* l2v4 = reinterpret_cast<const float4*>(l2v);  // 16-byte broadcasts
+                const int q0 = i * C::BM + 64 * h;  // query index of entry 0
+                const float2 c2 = make_float2(scale_log2, scale_log2);
+                const float4* l2v4 = reinterpret_cast<const float4*>(l2v);  // 16-byte broadcasts
 #pragma unroll
-                    for (int c = 0; c < 64; c += 4) {
-                        const float4 l = l2v4[c / 4];
+                for (int part = 0; part < 2; ++part) {
+                    uint32_t sr[32];
+                    tmem_ld32(t_lane + C::COL_S + 64 * h + 32 * part, sr);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 l = l2v4[(32 * part + c) / 4];
                         const float2 x0 = fma2(make_float2(__uint_as_float(sr[c]),
                                                            __uint_as_float(sr[c + 1])),
                                                c2, make_float2(-l.x, -l.y));
                         const float2 x1 = fma2(make_float2(__uint_as_float(sr[c + 2]),
                                                            __uint_as_float(sr[c + 3])),
                                                c2, make_float2(-l.z, -l.w));
-                        p[c] = ex2_approx(x0.x);
-                        p[c + 1] = ex2_approx(x0.y);
-                        p[c + 2] = ex2_approx(x1.x);
-                        p[c + 3] = ex2_approx(x1.y);
+                        p[32 * part + c] = ex2_approx(x0.x);
+                        p[32 * part + c + 1] = ex2_approx(x0.y);
+                        p[32 * part + c + 2] = ex2_approx(x1.x);
+                        p[32 * part + c + 3] = ex2_approx(x1.y);
                     }
                     if (key_pad || (CAUSAL && i == w.kt)) {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
+                        for (int c = 32 * part; c < 32 * part + 32; ++c)
                             if (key_pad || q0 + c < kglob) p[c] = 0.f;
                     }
-                }
-                {
-                    uint32_t pk[32];
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
-                    tmem_st32(t_lane + C::COL_S + 64 * h, pk);
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(p[32 * part + 2 * e], p[32 * part + 2 * e + 1]);
+                    tmem_st16(t_lane + C::COL_S + 64 * h + 16 * part, pk);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(part == 0 ? Bar::P_FULL : Bar::P_FULL2));
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(Bar::P_FULL));
 
                 // Phase dS: dS^T = P o (dP^T - D), BF16, over its dP^T columns.
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DP_FULL), g & 1, wc));

@@ -27,8 +27,9 @@
 //               two-deep ring of [Q_i | dO_i] stages plus the 128-entry LSE2 /
 //               D vectors.
 //   warps 1, 2  two MMA issuers (whole warps; one elected lane issues), so
-//               that one keeps the pipe fed while the other waits.  Each issuer overwrites only TMEM it alone reads,
-//               after those reads in its own issue order:
+//               that one keeps the pipe fed while the other waits.  Each
+//               issuer overwrites only TMEM it alone reads, after those reads
+//               in its own issue order:
 //                 issuer A: dV += P^T_t dO_t (A = P^T in TMEM, after P_FULL),
 //                           then S^T_t+1 = K Q_t+1^T over P^T_t;
 //                 issuer B: dK += dS^T_t Q_t (A = dS^T in TMEM, after DS_FULL),

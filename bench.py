@@ -60,12 +60,12 @@ def kernel_src_sha256(name: str) -> str:
 
 
 KERNEL_TRAFFIC = {
-    "fwd_bf16": {"bytes": 201437696 + 48240640,
-                "src_sha256": "a139f314cd8d4ab45530e24a33c32cc48cbad0241d8d214647d93dd4294b316d"},
-    "bwd_dkdv_bf16": {"bytes": 270631936 + 218725888,
-                     "src_sha256": "6f48d7d5919aa59826264a1142b2efec2cb8a059ed553d34b0038eaae99776fe"},
-    "bwd_dq_bf16": {"bytes": 336653312 + 111471104,
-                   "src_sha256": "a151369f758d3a826a996d484f59264857b0360ffa6be57da0dc1204940f2a69"},
+    "fwd_bf16": {"bytes": 201474816 + 48600832,
+                "src_sha256": "db52fa7847b0e62aa11f3a6a8de0059b861b3f5e4bade4f678bc2bfd2c421013"},
+    "bwd_dkdv_bf16": {"bytes": 270710784 + 218889728,
+                     "src_sha256": "022142edc8eb3ddcc3e561f1f01612c9e1fcc106955c6b21dfc78c536dee2816"},
+    "bwd_dq_bf16": {"bytes": 336706816 + 112085760,
+                   "src_sha256": "56e5a2e62909568e07e937ae80216c467b0926df3c4b7830c3d56f3d3461838a"},
 }
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps

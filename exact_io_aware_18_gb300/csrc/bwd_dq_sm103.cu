@@ -20,9 +20,10 @@
 //               The two rings free at different times, so each has its own
 //               thread, and each thread its own warp: two lanes of one warp
 //               that both spin on barriers share one instruction stream.
-//   warps 1, 10 two MMA issuers (one thread each; one thread alone issues a
-//               128 x 128 x 16 MMA no faster than the pipe runs it, so its
-//               barrier checks would idle the pipe).  Issuer A: S_0, S_1, then
+//   warps 1, 10 two MMA issuers, so that one keeps the pipe fed while the
+//               other waits (issuer B a whole warp with one elected lane;
+//               issuer A likewise without a causal mask, lane 0 alone with
+//               one, as measured fastest).  Issuer A: S_0, S_1, then
 //               per key tile j: dQ += dS_j K_j (A = dS_j in TMEM, after
 //               DS_FULL) and S_j+2 = Q K_j+2^T over dS_j.  Issuer B: (given O)
 //               D = diag(dO O^T) into the dQ columns, dP_0, then

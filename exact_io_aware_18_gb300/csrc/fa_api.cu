@@ -247,17 +247,19 @@ int dq_impl(const void* q, const void* k, const void* v, const void* o, const vo
     if (int rc = status_ptr(&status)) return rc;
     const long long BH = static_cast<long long>(B) * Hq;
     const long long BHkv = static_cast<long long>(B) * Hkv;
-    CUtensorMap tq, tk, tv, tdo, tdq, to;
+    CUtensorMap tq, tk, tv, tdo, to;
     if (int rc = make_map_bf16(&tq, q, d, N, BH)) return rc;
     if (int rc = make_map_bf16(&tk, k, d, N, BHkv)) return rc;
     if (int rc = make_map_bf16(&tv, v, d, N, BHkv)) return rc;
     if (int rc = make_map_bf16(&tdo, do_, d, N, BH)) return rc;
-    if (int rc = make_map_f32_out(&tdq, dq, d, N, BH)) return rc;
     if (o)
         if (int rc = make_map_bf16(&to, o, d, N, BH)) return rc;
-    fa::DqArgs a{&tq, &tk, &tv, &tdo, &tdq, o, o ? &to : nullptr, lse, delta_ws, lse2_ws, B, Hq, N, d,
+    unsigned int* work;
+    int sms = 0;
+    if (int rc = work_slot(&work, &sms)) return rc;
+    fa::DqArgs a{&tq, &tk, &tv, &tdo, dq, o, o ? &to : nullptr, lse, delta_ws, lse2_ws, B, Hq, N, d,
                  static_cast<int>(n_pad_of(N)), Hkv, causal ? 1 : 0, scale,
-                 scale * 1.4426950408889634f, status, g_timeout_ns.load()};
+                 scale * 1.4426950408889634f, status, g_timeout_ns.load(), work, sms};
     return launch_rc(fa::launch_bwd_dq_bf16(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -141,14 +141,14 @@ struct BwdArgs {
 
 cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t stream);
 
-// Backward dQ (BF16): one CTA per Q tile, loop over key tiles, dq written
-// once through an FP32 map like dK's.
+// Backward dQ (BF16): persistent CTAs that claim Q tiles, a loop over key
+// tiles per Q tile, dq written once through an FP32 map like dK's.
 struct DqArgs {
     const CUtensorMap* tm_q;
     const CUtensorMap* tm_k;
     const CUtensorMap* tm_v;
     const CUtensorMap* tm_do;
-    const CUtensorMap* tm_dq;
+    float* dq;  // FP32 [B,H,N,d], 16-byte aligned
     // o (bf16 [B,H,N,d]) and lse (float [B,H,N]) non-null: the kernel also
     // does the first backward step and writes delta and lse2; null: it reads
     // them as that step wrote them.  tm_o views o like tm_q views q (null
@@ -165,6 +165,8 @@ struct DqArgs {
     float scale_log2;
     unsigned int* status;
     unsigned long long timeout_ns;
+    unsigned int* work;  // tile counter of this launch, zero between launches
+    int num_sms;         // persistent grid size
 };
 
 cudaError_t launch_bwd_dq_bf16(const DqArgs& a, cudaStream_t stream);

@@ -184,8 +184,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// Makes this thread's generic-proxy shared-memory writes visible to the async
-// proxy (TMA stores, tcgen05.mma operand reads).
 // Stores four 32-bit words at a 16-byte aligned shared address.
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -209,6 +207,18 @@ __device__ __forceinline__ void st_row_sw128_f32(uint32_t box, int row, const ui
                      __float_as_uint(__uint_as_float(w[4 * c + 3]) * mul));
 }
 
+// Loads four FP32 words from a 16-byte aligned shared address.
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA stores, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

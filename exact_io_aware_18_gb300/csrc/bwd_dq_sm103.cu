@@ -81,7 +81,7 @@ struct DqCfg {
     static constexpr int OFF_BAR = OFF_STG + STG_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int OFF_ITEMS = OFF_BAR + BAR_BYTES;
-    static constexpr int LAYOUT_BYTES = OFF_ITEMS + QUEUE * 4;
+    static constexpr int LAYOUT_BYTES = OFF_ITEMS + QUEUE * 16;  // 4 ints per queued tile
     static constexpr int SMEM_BYTES =
         (LAYOUT_BYTES + 1024 <= kMaxDynSmem) ? LAYOUT_BYTES + 1024 : kMaxDynSmem;
     static_assert(LAYOUT_BYTES <= kMaxDynSmem, "dQ tiles do not fit in shared memory");
@@ -224,23 +224,32 @@ __global__ void __launch_bounds__(384, 1)
     const WaitCtx wc{status, timeout_ns, abort_flag};
     pdl_wait_then_release();
 
-    // Tile k of this CTA from the queue; -1 at the end of the work or when a
-    // wait gave up.  The lane form is for a single thread, the warp form for
-    // a whole warp (one arrival either way).
-    auto take_item = [&](int k) -> int {
-        const int slot = k % C::QUEUE;
-        if (!mbar_wait(bar(Bar::ITEM_FULL + slot), (k / C::QUEUE) & 1, wc)) return -1;
-        const int item = items[slot];
-        mbar_arrive(bar(Bar::ITEM_EMPTY + slot));
-        return item;
+    // Tile k of this CTA from the queue, as the claimer decoded it; qt = -1
+    // at the end of the work or when a wait gave up.  The lane form is for a
+    // single thread, the warp form for a whole warp (one arrival either way).
+    auto read_item = [&](int slot) -> Tile {
+        Tile t;
+        t.qt = items[4 * slot];
+        t.bh = items[4 * slot + 1];
+        t.bkv = items[4 * slot + 2];
+        t.n_kv = items[4 * slot + 3];
+        return t;
     };
-    auto take_item_warp = [&](int k) -> int {
+    auto take_item = [&](int k) -> Tile {
         const int slot = k % C::QUEUE;
-        if (!mbar_wait_warp(bar(Bar::ITEM_FULL + slot), (k / C::QUEUE) & 1, wc)) return -1;
-        const int item = __shfl_sync(0xffffffffu, items[slot], 0);
+        if (!mbar_wait(bar(Bar::ITEM_FULL + slot), (k / C::QUEUE) & 1, wc)) return Tile{-1, 0, 0, 0};
+        const Tile t = read_item(slot);
+        mbar_arrive(bar(Bar::ITEM_EMPTY + slot));
+        return t;
+    };
+    auto take_item_warp = [&](int k) -> Tile {
+        const int slot = k % C::QUEUE;
+        if (!mbar_wait_warp(bar(Bar::ITEM_FULL + slot), (k / C::QUEUE) & 1, wc)) return Tile{-1, 0, 0, 0};
+        const Tile t = read_item(slot);
+        __syncwarp();
         if (elect_one()) mbar_arrive(bar(Bar::ITEM_EMPTY + slot));
         __syncwarp();
-        return item;
+        return t;
     };
 
     if (warp == 0) {
@@ -307,11 +316,14 @@ __global__ void __launch_bounds__(384, 1)
                         if (t == static_cast<unsigned int>(n_items) - 1u) atomicExch(work, 0u);
                     }
                 }
-                if (item >= n_items) item = -1;
-                items[slot] = item;
+                // The tile is decoded once, here, off the other roles' paths.
+                const Tile t = item < n_items ? tile_of(item) : Tile{-1, 0, 0, 0};
+                items[4 * slot] = t.qt;
+                items[4 * slot + 1] = t.bh;
+                items[4 * slot + 2] = t.bkv;
+                items[4 * slot + 3] = t.n_kv;
                 mbar_arrive(bar(Bar::ITEM_FULL + slot));
-                if (item < 0) break;
-                const Tile t = tile_of(item);
+                if (t.qt < 0) break;
                 if (ok && k >= 1) ok = mbar_wait(bar(Bar::QD_EMPTY), (k - 1) & 1, wc);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(Bar::QD_FULL), 2 * C::TILE_BYTES);
@@ -358,9 +370,8 @@ __global__ void __launch_bounds__(384, 1)
             int vs = 0;
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int item = take_item(k);
-                if (item < 0) break;
-                const Tile t = tile_of(item);
+                const Tile t = take_item(k);
+                if (t.qt < 0) break;
                 for (int j = 0; ok && j < t.n_kv; ++j, ++vs) {
                     const int st = vs % C::NSV, use = vs / C::NSV;
                     if (use > 0) ok = mbar_wait(bar(Bar::V_EMPTY + st), (use - 1) & 1, wc);
@@ -400,9 +411,8 @@ __global__ void __launch_bounds__(384, 1)
             int gj = 0;  // key tiles of earlier Q tiles: S buffers and dS barriers
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int item = kWarpA ? take_item_warp(k) : take_item(k);
-                if (item < 0) break;
-                const Tile t = tile_of(item);
+                const Tile t = kWarpA ? take_item_warp(k) : take_item(k);
+                if (t.qt < 0) break;
                 if (fused) ++ks;  // the O slot, read by issuer B
                 const int k0 = ks;
                 ks += t.n_kv + (C::STG_IN_K ? 1 : 0);  // and the staging slot
@@ -477,9 +487,8 @@ __global__ void __launch_bounds__(384, 1)
         int ks = 0, vs = 0, gj = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            const int item = take_item_warp(k);
-            if (item < 0) break;
-            const Tile t = tile_of(item);
+            const Tile t = take_item_warp(k);
+            if (t.qt < 0) break;
             const int o_slot = ks;
             if (fused) ++ks;
             ks += t.n_kv + (C::STG_IN_K ? 1 : 0);
@@ -556,10 +565,29 @@ __global__ void __launch_bounds__(384, 1)
         int gj = 0;  // key tiles of earlier Q tiles
         int ks = 0;  // K slots, as the producer counts them (for the staging slot)
         bool ok = true;
-        for (int k = 0; ok; ++k) {
-            const int item = take_item_warp(k);
-            if (item < 0) break;
-            const Tile t = tile_of(item);
+        const float log2_scale = log2f(scale);
+        // A tile's per-row inputs (LSE given O, else D and LSE2) are loaded
+        // as soon as the tile is known: the next tile's while this one's
+        // epilogue runs.
+        struct RowIn {
+            float a, b;
+        };
+        auto row_in = [&](const Tile& u) -> RowIn {
+            RowIn v{0.f, 0.f};
+            if (u.qt < 0) return v;
+            const int qg = u.qt * C::BM + r;
+            if (fused) {
+                if (qg < N) v.a = lse[static_cast<long long>(u.bh) * N + qg];
+            } else {
+                const long long off = static_cast<long long>(u.bh) * n_pad + qg;
+                v.a = delta[off];
+                v.b = lse2[off];
+            }
+            return v;
+        };
+        Tile t = take_item_warp(0);
+        RowIn in = row_in(t);
+        for (int k = 0; ok && t.qt >= 0; ++k) {
             const int qt = t.qt, bh = t.bh;
             const int stg_pos = ks + (fused ? 1 : 0) + t.n_kv;  // this tile's staging slot
             ks = stg_pos + (C::STG_IN_K ? 1 : 0);
@@ -571,8 +599,6 @@ __global__ void __launch_bounds__(384, 1)
                 // (r, r) of dO O^T, which issuer B computes into the dQ
                 // columns; lane r of this warp's quarter finds it at column r.
                 const bool real = qglob < N;
-                // LSE is issued first, so its latency runs under the wait.
-                const float lse_r = real ? lse[static_cast<long long>(bh) * N + qglob] : 0.f;
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::D_FULL), k & 1, wc));
                 float dg = 0.f;
                 if (ok) {
@@ -586,17 +612,17 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 __syncwarp();
                 d_r = real ? dg : 0.f;
-                l2_r = real ? lse_r * 1.4426950408889634f : INFINITY;
+                l2_r = real ? in.a * 1.4426950408889634f : INFINITY;
                 if (h == 0) {
                     delta[voff] = d_r;
                     lse2[voff] = l2_r;
                 }
             } else {
-                d_r = delta[voff];
-                l2_r = lse2[voff];
+                d_r = in.a;
+                l2_r = in.b;
             }
             // P = 0 on padding rows (l2_r = +inf); log2(scale) folds scale into P.
-            const float neg_l2 = log2f(scale) - l2_r;
+            const float neg_l2 = log2_scale - l2_r;
             const float2 c2 = make_float2(scale_log2, scale_log2);
             const float2 neg_l2_2 = make_float2(neg_l2, neg_l2);
             const float2 neg_d2 = make_float2(-d_r, -d_r);  // dP - D as an addition of -D
@@ -657,6 +683,9 @@ __global__ void __launch_bounds__(384, 1)
                 if (lane == 0) mbar_arrive(bar(Bar::DS_FULL + (g & 1)));
             }
             gj += t.n_kv;
+            // The next tile now, so that its row inputs load under this epilogue.
+            const Tile tn = ok ? take_item_warp(k + 1) : Tile{-1, 0, 0, 0};
+            in = row_in(tn);
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(Bar::DQ_DONE), k & 1, wc));
             if (!ok) break;
             tc_fence_after();
@@ -708,6 +737,7 @@ __global__ void __launch_bounds__(384, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(Bar::STG_FREE));
             }
+            t = tn;
         }
     }
 

@@ -434,23 +434,27 @@ __device__ __forceinline__ void tmem_st_wait() {
 // Maps a linear CTA index to (tile, head) so that the CTAs resident at one
 // time work on a few heads (their shared operands stay in L2) while, inside
 // a group of heads, the heaviest tiles start first.  Heads are taken in
-// groups of `group`; inside a group the index runs over tiles in the order
-// given by `heavy_first_tile(k)` for k = 0, 1, ..., interleaving the heads.
+// groups of `group`; inside a group the index runs over the tiles (the last
+// tile first when reverse_tiles, the heaviest under a causal mask on the Q
+// side), interleaving the heads.
 struct TileHead {
     int tile;
     int head;
 };
 
-__device__ __forceinline__ TileHead grouped_order(long long lin, int BH, int n_tiles, int group,
+// 32-bit arithmetic throughout: the callers keep tiles x heads below 2^31,
+// and a 64-bit division is a long software routine on the critical path of
+// every role at every tile boundary.
+__device__ __forceinline__ TileHead grouped_order(int lin, int BH, int n_tiles, int group,
                                                    bool reverse_tiles) {
-    const long long per_group = static_cast<long long>(group) * n_tiles;
-    const int g = static_cast<int>(lin / per_group);
-    const int head0 = g * group;
+    const unsigned per_group = static_cast<unsigned>(group) * static_cast<unsigned>(n_tiles);
+    const unsigned g = static_cast<unsigned>(lin) / per_group;
+    const int head0 = static_cast<int>(g) * group;
     const int heads = min(group, BH - head0);  // the last group may be smaller
-    const long long r = lin - static_cast<long long>(g) * per_group;
-    const int k = static_cast<int>(r / heads);
-    const int h = static_cast<int>(r % heads);
-    return {reverse_tiles ? n_tiles - 1 - k : k, head0 + h};
+    const unsigned r = static_cast<unsigned>(lin) - g * per_group;
+    const unsigned k = r / static_cast<unsigned>(heads);
+    const int h = static_cast<int>(r - k * static_cast<unsigned>(heads));
+    return {reverse_tiles ? n_tiles - 1 - static_cast<int>(k) : static_cast<int>(k), head0 + h};
 }
 
 // ------------------------------------------------------------------ math

@@ -109,9 +109,15 @@ struct BwdBars {
     static constexpr int V_FULL = K_FULL + 1;
     static constexpr int K_EMPTY = V_FULL + 1;
     static constexpr int V_EMPTY = K_EMPTY + 1;
+    // A stage holds Q (with LSE2 and D) and dO, each with its own barriers:
+    // dO is last read by issuer A's dV, about one MMA group before Q's last
+    // reader, issuer B's dK, so the next dO loads that much earlier and Q's
+    // load, on the path to the next S^T, moves half the bytes.
     static constexpr int Q_FULL = V_EMPTY + 1;
-    static constexpr int Q_EMPTY = Q_FULL + NSQ;
-    static constexpr int S_FULL = Q_EMPTY + NSQ;
+    static constexpr int Q_EMPTY = Q_FULL + NSQ;   // S^T (A) and dK (B) done
+    static constexpr int DO_FULL = Q_EMPTY + NSQ;
+    static constexpr int DO_EMPTY = DO_FULL + NSQ;  // dP^T (B) and dV (A) done
+    static constexpr int S_FULL = DO_EMPTY + NSQ;
     static constexpr int DP_FULL = S_FULL + 1;
     // P^T is released in two parts (queries 0-31 and 64-95, then 32-63 and
     // 96-127), so that dV's first four products start while the second part
@@ -196,6 +202,8 @@ __global__ void __launch_bounds__(512, 1)
         for (int s = 0; s < C::NSQ; ++s) {
             mbar_init(bar(Bar::Q_FULL + s), 1);
             mbar_init(bar(Bar::Q_EMPTY + s), 2);  // one commit per issuer
+            mbar_init(bar(Bar::DO_FULL + s), 1);
+            mbar_init(bar(Bar::DO_EMPTY + s), 2);
         }
         mbar_init(bar(Bar::S_FULL), 1);
         mbar_init(bar(Bar::DP_FULL), 1);
@@ -291,7 +299,7 @@ __global__ void __launch_bounds__(512, 1)
         } else if (warp == 0) {
             // ------------------------------------------------------------ producer
             if (lane == 0) {
-                int g = 0, issued = 0, k_loads = 0, v_loads = 0;
+                int g = 0, issued = 0, issued_do = 0, k_loads = 0, v_loads = 0;
                 bool ok = true;
                 for (int k = 0; ok; ++k) {
                     const int item = take_item(k);
@@ -310,19 +318,28 @@ __global__ void __launch_bounds__(512, 1)
                     for (int t = 0; t < w.n_steps && ok; ++t, ++g) {
                         const int st = g % C::NSQ;
                         const int use = g / C::NSQ;
-                        if (use > 0) ok = mbar_wait(bar(Bar::Q_EMPTY + st), (use - 1) & 1, wc);
-                        if (!ok) break;
                         const int i = w.i0 + t % w.n_q;
                         const int bh = w.bhq0 + t / w.n_q;  // query head
+                        const long long voff = static_cast<long long>(bh) * n_pad + i * C::BM;
+                        // dO first: its half of the stage frees first.
+                        if (use > 0) ok = mbar_wait(bar(Bar::DO_EMPTY + st), (use - 1) & 1, wc);
+                        if (!ok) break;
+                        const uint32_t fo = bar(Bar::DO_FULL + st);
+                        mbar_arrive_expect_tx(fo, C::TILE_BYTES);
+                        for (int kb = 0; kb < C::KB; ++kb)
+                            tma_load_3d(do_of(st) + kb * C::BOX_BYTES, &tm_do, fo, kb * 64,
+                                        i * C::BM, bh);
+                        issued_do = g + 1;
+                        // Q with LSE2 and D: the math warps read D in the dS
+                        // phase, which dK (Q's last reader) follows, while dV
+                        // (dO's last reader) may end before it.
+                        if (use > 0) ok = mbar_wait(bar(Bar::Q_EMPTY + st), (use - 1) & 1, wc);
+                        if (!ok) break;
                         const uint32_t fb = bar(Bar::Q_FULL + st);
-                        mbar_arrive_expect_tx(fb, C::STAGE_BYTES + 1024);
-                        for (int kb = 0; kb < C::KB; ++kb) {
+                        mbar_arrive_expect_tx(fb, C::TILE_BYTES + 1024);
+                        for (int kb = 0; kb < C::KB; ++kb)
                             tma_load_3d(q_of(st) + kb * C::BOX_BYTES, &tm_q, fb, kb * 64,
                                         i * C::BM, bh);
-                            tma_load_3d(do_of(st) + kb * C::BOX_BYTES, &tm_do, fb, kb * 64,
-                                        i * C::BM, bh);
-                        }
-                        const long long voff = static_cast<long long>(bh) * n_pad + i * C::BM;
                         bulk_load(s_vec + st * 1024, lse2 + voff, 512, fb);
                         bulk_load(s_vec + st * 1024 + 512, delta + voff, 512, fb);
                         issued = g + 1;
@@ -343,6 +360,8 @@ __global__ void __launch_bounds__(512, 1)
                     mbar_wait_drain(bar(Bar::K_FULL), (k_loads - 1) & 1, timeout_ns);
                 if (v_loads > 0)
                     mbar_wait_drain(bar(Bar::V_FULL), (v_loads - 1) & 1, timeout_ns);
+                for (int t = (issued_do > C::NSQ ? issued_do - C::NSQ : 0); t < issued_do; ++t)
+                    mbar_wait_drain(bar(Bar::DO_FULL + t % C::NSQ), (t / C::NSQ) & 1, timeout_ns);
                 for (int t = (issued > C::NSQ ? issued - C::NSQ : 0); t < issued; ++t)
                     mbar_wait_drain(bar(Bar::Q_FULL + t % C::NSQ), (t / C::NSQ) & 1, timeout_ns);
             }
@@ -369,12 +388,18 @@ __global__ void __launch_bounds__(512, 1)
                 const uint32_t c_acc = issuer_a ? C::COL_DV : C::COL_DK;   // dV or dK
                 const uint32_t c_a = issuer_a ? C::COL_S : C::COL_DP;      // P^T or dS^T
                 const int ready_bar = issuer_a ? Bar::P_FULL : Bar::DS_FULL;
+                // Stage halves: the first GEMM's B operand (Q for A, dO for
+                // B) and the accumulation's (dO for A, Q for B).
+                const int first_full = issuer_a ? Bar::Q_FULL : Bar::DO_FULL;
+                const int first_empty = issuer_a ? Bar::Q_EMPTY : Bar::DO_EMPTY;
+                const int acc_full = issuer_a ? Bar::DO_FULL : Bar::Q_FULL;
+                const int acc_empty = issuer_a ? Bar::DO_EMPTY : Bar::Q_EMPTY;
                 const int full_bar = issuer_a ? Bar::S_FULL : Bar::DP_FULL;
                 const int free_bar = issuer_a ? Bar::DV_FREE : Bar::DK_FREE;
                 // First GEMM of step g: S^T = K Q^T (A) or dP^T = V dO^T (B).
                 auto issue_first = [&](int g) -> bool {
                     const int st = g % C::NSQ;
-                    if (!mbar_wait_warp(bar(Bar::Q_FULL + st), (g / C::NSQ) & 1, wc)) return false;
+                    if (!mbar_wait_warp(bar(first_full + st), (g / C::NSQ) & 1, wc)) return false;
                     tc_fence_after();
                     const uint64_t d_b = desc_advance(d_kmaj0, st * C::STAGE_BYTES);
 #pragma unroll
@@ -385,7 +410,10 @@ __global__ void __launch_bounds__(512, 1)
                         if (elect_one()) mma_ss(tmem + c_first, ad, bd, id_sp, kk > 0);
                         __syncwarp();
                     }
-                    if (elect_one()) tc_commit(bar(full_bar));
+                    if (elect_one()) {
+                        tc_commit(bar(full_bar));
+                        tc_commit(bar(first_empty + st));  // this half of the stage is read
+                    }
                     __syncwarp();
                     return true;
                 };
@@ -407,6 +435,8 @@ __global__ void __launch_bounds__(512, 1)
                         // The item's first accumulation overwrites dV (dK): the
                         // epilogue must have read the previous item's out.
                         if (ok && t == 0 && k >= 1) ok = mbar_wait_warp(bar(free_bar), (k - 1) & 1, wc);
+                        // The accumulation's own operand half of the stage.
+                        ok = ok && mbar_wait_warp(bar(acc_full + st), (g / C::NSQ) & 1, wc);
                         // Issuer B holds dK_t and dP^T_t+1 until issuer A's S^T_t+1 is
                         // done: A's dV_t, S^T_t+1 lead to the next P phase and should
                         // not share the pipe; B's pair then runs during that P phase.
@@ -443,7 +473,7 @@ __global__ void __launch_bounds__(512, 1)
                         }
                         if (!ok) break;
                         // This issuer no longer reads stage g.
-                        if (elect_one()) tc_commit(bar(Bar::Q_EMPTY + st));
+                        if (elect_one()) tc_commit(bar(acc_empty + st));
                         __syncwarp();
                         if (t + 1 < w.n_steps) {
                             ok = issue_first(g + 1);

@@ -60,12 +60,12 @@ def kernel_src_sha256(name: str) -> str:
 
 
 KERNEL_TRAFFIC = {
-    "fwd_bf16": {"bytes": 201474816 + 48600832,
-                "src_sha256": "db52fa7847b0e62aa11f3a6a8de0059b861b3f5e4bade4f678bc2bfd2c421013"},
-    "bwd_dkdv_bf16": {"bytes": 270710784 + 218889728,
-                     "src_sha256": "022142edc8eb3ddcc3e561f1f01612c9e1fcc106955c6b21dfc78c536dee2816"},
-    "bwd_dq_bf16": {"bytes": 336706816 + 112085760,
-                   "src_sha256": "a18b00fbbd24e86654d3249349066a7884cd311dec091a05802f93cc6d2433be"},
+    "fwd_bf16": {"bytes": 201428992 + 48713984,
+                "src_sha256": "0668d7135f5a23a0ec13a674e40f058608bcfefe73edcb6f04c7b8ad31d6bef1"},
+    "bwd_dkdv_bf16": {"bytes": 270753024 + 218957568,
+                     "src_sha256": "2ba0abd8b222b5bd3cd8b2d0f7371a1441715e7815cb4124030db261d4bbbcb8"},
+    "bwd_dq_bf16": {"bytes": 336913920 + 109573120,
+                   "src_sha256": "8cdae68490484523b76845e4b4735fb722f86933aa3f3baebda761aee66c8d0a"},
 }
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps

@@ -389,19 +389,14 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer A
         // Each issuer is a whole warp: every lane waits and computes the
-        // operands, one elected lane issues the MMAs and commits.  Under a
-        // causal mask issuer A is lane 0 alone instead: measured both ways,
-        // the whole warp made dQ 5 % faster without the mask and 2-3 % slower
-        // with it (the cause was not found).
-        constexpr bool kWarpA = !CAUSAL;
-        auto wait_a = [&](uint32_t b, uint32_t parity) {
-            return kWarpA ? mbar_wait_warp(b, parity, wc) : mbar_wait(b, parity, wc);
-        };
-        auto lead_a = [&]() { return kWarpA ? elect_one() : true; };
-        auto sync_a = [&]() {
-            if (kWarpA) __syncwarp();
-        };
-        if (kWarpA || lane == 0) {
+        // operands, one elected lane issues the MMAs and commits.  (Under a
+        // causal mask a lone-lane issuer A once measured faster; that was
+        // while the mask test sat inside the exponential loop.  With the
+        // mask in its own pass the whole warp is 2.5-5 % faster there too.)
+        auto wait_a = [&](uint32_t b, uint32_t parity) { return mbar_wait_warp(b, parity, wc); };
+        auto lead_a = [&]() { return elect_one(); };
+        auto sync_a = [&]() { __syncwarp(); };
+        {
             constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // S: both K-major
             constexpr uint32_t id_q = idesc_bf16(128, D, 0, 1);    // dQ: B MN-major
             const uint64_t d_q = smem_desc_sw128(s_q, 16, 1024);
@@ -411,7 +406,7 @@ __global__ void __launch_bounds__(384, 1)
             int gj = 0;  // key tiles of earlier Q tiles: S buffers and dS barriers
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const Tile t = kWarpA ? take_item_warp(k) : take_item(k);
+                const Tile t = take_item_warp(k);
                 if (t.qt < 0) break;
                 if (fused) ++ks;  // the O slot, read by issuer B
                 const int k0 = ks;
@@ -746,7 +741,7 @@ __global__ void __launch_bounds__(384, 1)
     // The commits come from the lane that issued each warp's MMAs.
     if (warp == 10 && elect_one()) tc_commit(bar(Bar::DONE));
     if (warp == 1) {
-        if (CAUSAL ? lane == 0 : elect_one()) {
+        if (elect_one()) {
             tc_commit(bar(Bar::DONE));  // both issuers' MMAs have completed
             mbar_wait_drain(bar(Bar::DONE), 0, timeout_ns);
         }

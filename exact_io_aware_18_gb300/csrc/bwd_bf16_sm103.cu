@@ -578,9 +578,11 @@ __global__ void __launch_bounds__(512, 1)
                         p[32 * part + c + 3] = ex2_approx(x1.y);
                     }
                     if (key_pad || (CAUSAL && i == w.kt)) {
+                        // Queries before the key (causal), or every query of a
+                        // padding key: entry c is zeroed while c < lim.
+                        const int lim = key_pad ? 64 : kglob - q0;
 #pragma unroll
-                        for (int c = 32 * part; c < 32 * part + 32; ++c)
-                            if (key_pad || q0 + c < kglob) p[c] = 0.f;
+                        for (int c = 32 * part; c < 32 * part + 32; ++c) p[c] = c < lim ? 0.f : p[c];
                     }
                     uint32_t pk[16];
 #pragma unroll

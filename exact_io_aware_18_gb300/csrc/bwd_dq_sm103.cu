@@ -653,11 +653,11 @@ __global__ void __launch_bounds__(384, 1)
                     // The mask in a pass of its own behind one branch: laid
                     // into the loop above, it is paid on every key tile.
                     if (masked) {
+                        // Keys past the row (causal) or past N: entry c is
+                        // kept while c < lim.
+                        const int lim = (CAUSAL ? min(qglob + 1, N) : N) - (key0 + 32 * ch);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const int key = key0 + 32 * ch + c;
-                            if ((CAUSAL && key > qglob) || key >= N) p[c] = 0.f;
-                        }
+                        for (int c = 0; c < 32; ++c) p[c] = c < lim ? p[c] : 0.f;
                     }
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {

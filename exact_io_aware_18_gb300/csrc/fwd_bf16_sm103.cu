@@ -542,11 +542,11 @@ __global__ void __launch_bounds__(384, 1)
                     }
                     const int key0 = j * C::BN + 64 * h;  // key index of entry 0
                     if ((CAUSAL && j == qt) || key0 + 64 > Nk) {
+                        // Keys past the row (causal) or past Nk: entry c is
+                        // kept while c < lim.
+                        const int lim = (CAUSAL ? min(grow + 1, Nk) : Nk) - key0;
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            const int key = key0 + c;
-                            if ((CAUSAL && key > grow) || key >= Nk) s[c] = -INFINITY;
-                        }
+                        for (int c = 0; c < 64; ++c) s[c] = c < lim ? s[c] : -INFINITY;
                     }
                     // Four independent running maxima, then their max: a chain
                     // of 8 three-input max instructions instead of 32.

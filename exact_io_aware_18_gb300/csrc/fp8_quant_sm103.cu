@@ -21,12 +21,12 @@
 // ..., d/2) maps the pair (y_i, y_{i+h}) of each block of 2h to
 // (y_i + y_{i+h}, y_i - y_{i+h}).
 //
-// Mapping: persistent CTAs of 128 threads, two per SM, each thread one row of
-// the current tile, so the whole transform runs in its registers.  Three
-// tile buffers per CTA: thread 0 keeps the loads of the next two tiles in
-// flight while the current one is transformed, and each tile's codes are
-// written over the first half of its own buffer (its BF16 rows are all in
-// registers by then) and leave by TMA store.  With 128-byte swizzled boxes on
+// Mapping: persistent CTAs of 128 threads, three per SM, each thread one row
+// of the current tile, so the whole transform runs in its registers.  Two
+// tile buffers per CTA: thread 0 keeps the load of the next tile in flight
+// while the current one is transformed, and each tile's codes are written
+// over the first half of its own buffer (its BF16 rows are all in registers
+// by then) and leave by TMA store.  With 128-byte swizzled boxes on
 // both sides, a warp's 16-byte shared-memory accesses to 32 different rows hit
 // distinct banks.  Stages h >= 2 pair whole float2 registers and use the packed FP32
 // instructions; stage 1 pairs the two halves of each float2.
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm)
             tma_load_3d(dst + kb * C::BOX_BYTES, &tm_x, bar_full + 8 * buf, kb * 64,
                         tile * kTileRows, bh);
     };
-    // Tile `it` of this CTA is item blockIdx.x + it * gridDim.x, in buffer it % 3.
+    // Tile `it` of this CTA is item blockIdx.x + it * gridDim.x, in buffer it % NBUF.
     int loads = 0;
     if (tid == 0) {
         for (int t = 0; t < C::NBUF - 1; ++t) {

@@ -60,12 +60,12 @@ def kernel_src_sha256(name: str) -> str:
 
 
 KERNEL_TRAFFIC = {
-    "fwd_bf16": {"bytes": 201428992 + 48713984,
-                "src_sha256": "0668d7135f5a23a0ec13a674e40f058608bcfefe73edcb6f04c7b8ad31d6bef1"},
-    "bwd_dkdv_bf16": {"bytes": 270753024 + 218957568,
-                     "src_sha256": "2ba0abd8b222b5bd3cd8b2d0f7371a1441715e7815cb4124030db261d4bbbcb8"},
-    "bwd_dq_bf16": {"bytes": 336913920 + 109573120,
-                   "src_sha256": "8cdae68490484523b76845e4b4735fb722f86933aa3f3baebda761aee66c8d0a"},
+    "fwd_bf16": {"bytes": 201415424 + 48825344,
+                "src_sha256": "3ee93ae23836f802cfe9a642d0813cac954fcc5cc3db0085cce360476325f2c9"},
+    "bwd_dkdv_bf16": {"bytes": 270681344 + 218626304,
+                     "src_sha256": "ed50b3cae5d19694243f7a067a00e7002cb60b0111779e80c16265435a269a46"},
+    "bwd_dq_bf16": {"bytes": 336928256 + 109873408,
+                   "src_sha256": "e7bb6658e209361ca34a70b776f13af9f29b5d6280ce2df865887e2d83294bba"},
 }
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps

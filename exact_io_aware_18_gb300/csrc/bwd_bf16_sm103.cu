@@ -84,13 +84,17 @@ struct BwdCfg {
     static constexpr int OFF_V = OFF_K + TILE_BYTES;
     static constexpr int OFF_STAGE = OFF_V + TILE_BYTES;
     static constexpr int OFF_VEC = OFF_STAGE + NSQ * STAGE_BYTES;  // NSQ x (lse2, delta)
-    static constexpr int OFF_STG = OFF_VEC + NSQ * 1024;           // 4 epilogue boxes of 4 KB
-    static constexpr int OFF_BAR = OFF_STG + 4 * 4096;
+    static constexpr int NBOX = 8;  // epilogue boxes of 4 KB, two per epilogue warp
+    static constexpr int OFF_STG = OFF_VEC + NSQ * 1024;
+    static constexpr int OFF_BAR = OFF_STG + NBOX * 4096;
     static constexpr int BAR_BYTES = 256;
     static constexpr int OFF_ITEMS = OFF_BAR + BAR_BYTES;
     static constexpr int LAYOUT_BYTES = OFF_ITEMS + QUEUE * 4;
-    static constexpr int SMEM_BYTES = LAYOUT_BYTES + 1024;  // + alignment slack
-    static_assert(SMEM_BYTES <= kMaxDynSmem, "backward tiles do not fit in shared memory");
+    // Alignment slack of up to 1 KB, as much as the limit leaves (the dynamic
+    // window starts 1024-byte aligned in practice; the kernel checks).
+    static constexpr int SMEM_BYTES =
+        (LAYOUT_BYTES + 1024 <= kMaxDynSmem) ? LAYOUT_BYTES + 1024 : kMaxDynSmem;
+    static_assert(LAYOUT_BYTES <= kMaxDynSmem, "backward tiles do not fit in shared memory");
     static_assert(OFF_STG % 1024 == 0, "swizzled staging boxes need 1024-byte alignment");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
@@ -488,10 +492,14 @@ __global__ void __launch_bounds__(512, 1)
         } else {
             // ------------------------------------------------------------ epilogue
             // Warp e (of warps 12-15) owns TMEM lanes 32 (e % 4) .. +32: rows
-            // of dV, then of dK, 32 columns (one 4 KB box) at a time.
+            // of dV, then of dK, 32 columns (one 4 KB box) at a time, through
+            // two boxes in turn.  A box is rewritten once the store issued
+            // from it two chunks earlier has read it, so the reads out of
+            // TMEM run a chunk ahead of the SM's write path and each
+            // accumulator is released that much sooner.
             const int wq = warp & 3;
             const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-            const uint32_t box = s_base + C::OFF_STG + static_cast<uint32_t>(wq * 4096);
+            const uint32_t box0 = s_base + C::OFF_STG + static_cast<uint32_t>(wq * 2 * 4096);
             constexpr int NCH = D / 32;  // 32-column chunks of dV (and of dK)
             bool ok = true;
             for (int k = 0; ok; ++k) {
@@ -512,13 +520,18 @@ __global__ void __launch_bounds__(512, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(c == NCH - 1 ? Bar::DV_FREE : Bar::DK_FREE));
                     }
-                    if (lane == 0) bulk_wait_read_all();  // the box is free again
+                    // Every chunk commits one group (empty past N), so "at
+                    // most one group still reading" frees this chunk's box.
+                    if (lane == 0) bulk_wait_read_allow1();
                     __syncwarp();
+                    const uint32_t box = box0 + static_cast<uint32_t>((c & 1) * 4096);
                     st_row_sw128_f32(box, lane, a, c < NCH ? 1.f : scale);
                     fence_async_smem();
                     __syncwarp();
-                    if (lane == 0 && row0 < N) {
-                        tma_store_3d(c < NCH ? &tm_dv : &tm_dk, box, 32 * (c % NCH), row0, w.bkv);
+                    if (lane == 0) {
+                        if (row0 < N)
+                            tma_store_3d(c < NCH ? &tm_dv : &tm_dk, box, 32 * (c % NCH), row0,
+                                         w.bkv);
                         bulk_commit();
                     }
                 }

@@ -159,6 +159,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// Waits until at most the most recent bulk group of this thread is still
+// reading its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_allow1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

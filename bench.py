@@ -60,12 +60,12 @@ def kernel_src_sha256(name: str) -> str:
 
 
 KERNEL_TRAFFIC = {
-    "fwd_bf16": {"bytes": 201415424 + 48825344,
-                "src_sha256": "3ee93ae23836f802cfe9a642d0813cac954fcc5cc3db0085cce360476325f2c9"},
-    "bwd_dkdv_bf16": {"bytes": 270681344 + 218626304,
-                     "src_sha256": "ed50b3cae5d19694243f7a067a00e7002cb60b0111779e80c16265435a269a46"},
-    "bwd_dq_bf16": {"bytes": 336928256 + 109873408,
-                   "src_sha256": "e7bb6658e209361ca34a70b776f13af9f29b5d6280ce2df865887e2d83294bba"},
+    "fwd_bf16": {"bytes": 201412992 + 45501952,
+                "src_sha256": "1ed9d3560e5c81657b391435a08054e7386f83624100054113c9f9aa25d32a9c"},
+    "bwd_dkdv_bf16": {"bytes": 270670848 + 218552320,
+                     "src_sha256": "4a6dfcaf6b20e7f86181ee79e116ff10fe2b4e14b40e6ae7ee3dbf86424442b4"},
+    "bwd_dq_bf16": {"bytes": 336796544 + 108008704,
+                   "src_sha256": "46d7f5abc8dff95c2ffbc74968e0bd838bf5b7537d881dcd6cebda595327883f"},
 }
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps

@@ -189,6 +189,23 @@ def test_bf16_multi_tile_full(fa, dev, N, d, causal):
     _check_grads(got, refs, np.arange(B * H), B, H, N, d)  # the composed chain
 
 
+@pytest.mark.parametrize("d,causal", [(128, True), (128, False), (64, True), (64, False)])
+def test_backward_many_tiles_per_cta(fa, dev, d, causal):
+    """More Q tiles and key tiles than SMs, so that every persistent CTA of
+    the dQ and dK/dV kernels runs several tiles in a row (the switches from
+    one tile to the next, the ring positions and staging slots that run
+    across tiles), with a ragged last tile: whole sampled heads of the
+    composed forward -> backward chain against the oracle."""
+    B, H, N = 4, 20, 520
+    x = inputs(90 + d + int(causal), B, H, N, d)
+    s = scale_for(d)
+    got = _bf16_run(fa, dev, x, causal, s)
+    heads = np.array([0, 23, 41, 79])
+    refs = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], causal, s, heads=heads,
+                                o_storage="bf16")[:3]
+    _check_grads(got, refs, heads, B, H, N, d)
+
+
 def test_config_b2_h8_n1024_d64_full(fa, dev):
     """bf16 forward, B=2 H=8 N=1024 d=64, non-causal, seed 1: every output."""
     B, H, N, d = 2, 8, 1024, 64

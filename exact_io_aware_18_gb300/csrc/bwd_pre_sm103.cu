@@ -11,9 +11,10 @@
 //
 // Each thread reads 16-byte vectors, 8 bf16 of O and of dO; d/8 threads share
 // a row and reduce with warp shuffles.  A warp owns 32 / (d/8) consecutive
-// rows per group and issues the loads of two groups before it reduces any,
-// so that enough bytes are in flight to keep HBM busy; warps stride over the
-// rows with the whole grid (at most full occupancy on every SM).
+// rows per group and issues the loads of two groups (LSE included) before it
+// reduces any, so that enough bytes are in flight to keep HBM busy and no
+// load waits on another; warps stride over the rows with the whole grid (at
+// most full occupancy on every SM).
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -42,21 +43,26 @@ __global__ void __launch_bounds__(kPreThreads)
     // a warp's batch exists and the shuffles below see the whole warp.
     for (long long r0 = warp_id * (RW * U); r0 < total_rows; r0 += n_warps * (RW * U)) {
         uint4 a[U], b[U];
+        float l[U];
         bool real[U];
-        long long row[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const long long r = r0 + u * RW + lane / TPR;
-            const long long bh = r / n_pad;
-            const int i = static_cast<int>(r - bh * n_pad);
+            // n_pad is a multiple of 128 and r / 128 fits 32 bits (tiles x
+            // heads < 2^31): a 32-bit division finds the head.
+            const unsigned int tr = static_cast<unsigned int>(r >> 7);
+            const unsigned int bh = tr / static_cast<unsigned int>(n_pad >> 7);
+            const int i = static_cast<int>(r - static_cast<long long>(bh) * n_pad);
             real[u] = i < N;
-            row[u] = bh * N + i;
+            const long long row = static_cast<long long>(bh) * N + i;
             if (real[u]) {
-                a[u] = o[row[u] * (D / 8) + sub];
-                b[u] = dO[row[u] * (D / 8) + sub];
+                a[u] = o[row * (D / 8) + sub];
+                b[u] = dO[row * (D / 8) + sub];
+                l[u] = lse[row];
             } else {
                 a[u] = make_uint4(0u, 0u, 0u, 0u);
                 b[u] = a[u];
+                l[u] = 0.f;
             }
         }
 #pragma unroll
@@ -77,7 +83,7 @@ __global__ void __launch_bounds__(kPreThreads)
             if (sub == 0) {
                 const long long r = r0 + u * RW + lane / TPR;
                 delta[r] = real[u] ? part : 0.f;
-                lse2[r] = real[u] ? lse[row[u]] * 1.4426950408889634f : INFINITY;
+                lse2[r] = real[u] ? l[u] * 1.4426950408889634f : INFINITY;
             }
         }
     }

@@ -142,7 +142,7 @@ struct BwdArgs {
 cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t stream);
 
 // Backward dQ (BF16): persistent CTAs that claim Q tiles, a loop over key
-// tiles per Q tile, dq written once through an FP32 map like dK's.
+// tiles per Q tile, dq written once (FP32, from a staging box per warp).
 struct DqArgs {
     const CUtensorMap* tm_q;
     const CUtensorMap* tm_k;

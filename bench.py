@@ -793,10 +793,15 @@ def run_reference(args):
     n_heads = max(1, min(B * H, cores))
     x = fa_inputs.attention_inputs(SEED, B, H, N, D, "bf16")
     # A step is the oracle on a sample of whole heads, seconds of CPU work, so
-    # the run is bounded in time: one warm-up step measures it, and at most
-    # as many timed steps as fit in REFERENCE_BUDGET_S run (never more than
-    # --steps).  The line reports both counts.
+    # the run is bounded in time: the first warm-up step measures it, the rest
+    # of --warmup run while they fit in a quarter of REFERENCE_BUDGET_S, and at
+    # most as many timed steps as fit in REFERENCE_BUDGET_S run (never more
+    # than --steps).  The line reports the counts run and requested.
     t_warm, _ = oracle_step_sample(x, n_heads)
+    warmup = 1
+    while warmup < args.warmup and (warmup + 1) * t_warm <= REFERENCE_BUDGET_S / 4:
+        oracle_step_sample(x, n_heads)
+        warmup += 1
     steps = max(1, min(args.steps, int(REFERENCE_BUDGET_S / max(t_warm, 1e-3))))
     total_s, total_f = 0.0, 0.0
     for _ in range(steps):
@@ -811,7 +816,7 @@ def run_reference(args):
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": steps,
-        "warmup": 1,
+        "warmup": warmup,
         "steps_requested": args.steps,
         "warmup_requested": args.warmup,
         "ms_per_step": round(1e3 * total_s / steps, 3),

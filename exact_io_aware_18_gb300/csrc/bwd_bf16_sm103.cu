@@ -667,9 +667,7 @@ cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_tiles = (a.N + C::BN - 1) / C::BN;
-    // Enough heads per group that a group fills about one wave of items.
-    int group = 128 / n_tiles;
-    if (group < 1) group = 1;
+    const int group = claim_group(n_tiles, CAUSAL);
     const long long n_items = static_cast<long long>(a.B) * a.Hkv * n_tiles;
     const int grid = static_cast<int>(n_items < a.num_sms ? n_items : a.num_sms);
     e = launch_overlapped(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tm_q,

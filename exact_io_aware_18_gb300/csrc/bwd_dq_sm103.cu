@@ -759,8 +759,7 @@ cudaError_t launch_t(const DqArgs& a, cudaStream_t stream) {
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_tiles = (a.N + C::BM - 1) / C::BM;
-    int group = 128 / n_tiles;
-    if (group < 1) group = 1;
+    const int group = claim_group(n_tiles, CAUSAL);
     // Persistent: one CTA per SM (at most one per Q tile) claims Q tiles.
     const long long n_items = static_cast<long long>(a.B) * a.H * n_tiles;
     const int grid = static_cast<int>(n_items < a.num_sms ? n_items : a.num_sms);

@@ -727,9 +727,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int n_tiles = (a.N + C::BM - 1) / C::BM;
-    // Enough heads per group that a group fills about one wave of tiles.
-    int group = 128 / n_tiles;
-    if (group < 1) group = 1;
+    const int group = claim_group(n_tiles, CAUSAL);
     const long long n_items = static_cast<long long>(a.B) * a.H * n_tiles * a.n_splits;
     const int grid = static_cast<int>(n_items < a.num_sms ? n_items : a.num_sms);
     e = launch_overlapped(

@@ -60,12 +60,12 @@ def kernel_src_sha256(name: str) -> str:
 
 
 KERNEL_TRAFFIC = {
-    "fwd_bf16": {"bytes": 201412992 + 45501952,
-                "src_sha256": "1ed9d3560e5c81657b391435a08054e7386f83624100054113c9f9aa25d32a9c"},
-    "bwd_dkdv_bf16": {"bytes": 270670848 + 218552320,
-                     "src_sha256": "4a6dfcaf6b20e7f86181ee79e116ff10fe2b4e14b40e6ae7ee3dbf86424442b4"},
-    "bwd_dq_bf16": {"bytes": 336796544 + 108008704,
-                   "src_sha256": "46d7f5abc8dff95c2ffbc74968e0bd838bf5b7537d881dcd6cebda595327883f"},
+    "fwd_bf16": {"bytes": 201416576 + 45444864,
+                "src_sha256": "9ba5d9b7326139ffba4fa3338bd3f4820dc74b5165666d34e1c67d6c5e69743b"},
+    "bwd_dkdv_bf16": {"bytes": 270739712 + 215204736,
+                     "src_sha256": "52cb748f4f5dbe0285a2f6e4646a375b09c973419bd1b8dc981c174d0c9db3a3"},
+    "bwd_dq_bf16": {"bytes": 336833024 + 108038016,
+                   "src_sha256": "f60af3f7f29555b610dd3f2170c3b0d832708633e4b39ef9e69d552cf3659351"},
 }
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps

@@ -166,7 +166,9 @@ __global__ void __launch_bounds__(384, 1)
         int qt, bh, bkv, n_kv;
     };
     auto tile_of = [&](int item) -> Tile {
-        const TileHead th = grouped_order(item, BH, n_tiles, group, true);
+        // Head groups in reverse: the forward before this kernel walks them
+        // forwards, so the first Q tiles here find their Q, K, V and O in L2.
+        const TileHead th = grouped_order(item, BH, n_tiles, group, true, true);
         Tile t;
         t.qt = th.tile;
         t.bh = th.head;

@@ -442,7 +442,10 @@ __device__ __forceinline__ void tmem_st_wait() {
 // a group of heads, the heaviest tiles start first.  Heads are taken in
 // groups of `group`; inside a group the index runs over the tiles (the last
 // tile first when reverse_tiles, the heaviest under a causal mask on the Q
-// side), interleaving the heads.
+// side), interleaving the heads.  With reverse_groups the groups run from the
+// last one back (the last group, which may hold fewer heads, first), so that
+// a kernel that follows one walking the groups forwards starts on the heads
+// whose tiles that kernel touched last, while they are still in L2.
 struct TileHead {
     int tile;
     int head;
@@ -452,12 +455,33 @@ struct TileHead {
 // and a 64-bit division is a long software routine on the critical path of
 // every role at every tile boundary.
 __device__ __forceinline__ TileHead grouped_order(int lin, int BH, int n_tiles, int group,
-                                                   bool reverse_tiles) {
+                                                   bool reverse_tiles,
+                                                   bool reverse_groups = false) {
     const unsigned per_group = static_cast<unsigned>(group) * static_cast<unsigned>(n_tiles);
-    const unsigned g = static_cast<unsigned>(lin) / per_group;
-    const int head0 = static_cast<int>(g) * group;
-    const int heads = min(group, BH - head0);  // the last group may be smaller
-    const unsigned r = static_cast<unsigned>(lin) - g * per_group;
+    const unsigned ulin = static_cast<unsigned>(lin);
+    int head0, heads;
+    unsigned r;
+    if (!reverse_groups) {
+        const unsigned g = ulin / per_group;
+        head0 = static_cast<int>(g) * group;
+        heads = min(group, BH - head0);  // the last group may be smaller
+        r = ulin - g * per_group;
+    } else {
+        const int last0 = ((BH - 1) / group) * group;  // first head of the last group
+        const unsigned first_items =
+            static_cast<unsigned>(BH - last0) * static_cast<unsigned>(n_tiles);
+        if (ulin < first_items) {
+            head0 = last0;
+            heads = BH - last0;
+            r = ulin;
+        } else {
+            const unsigned rest = ulin - first_items;
+            const unsigned g = rest / per_group;  // full groups before the last one, backwards
+            head0 = last0 - (static_cast<int>(g) + 1) * group;
+            heads = group;
+            r = rest - g * per_group;
+        }
+    }
     const unsigned k = r / static_cast<unsigned>(heads);
     const int h = static_cast<int>(r - k * static_cast<unsigned>(heads));
     return {reverse_tiles ? n_tiles - 1 - static_cast<int>(k) : static_cast<int>(k), head0 + h};

@@ -60,12 +60,12 @@ def kernel_src_sha256(name: str) -> str:
 
 
 KERNEL_TRAFFIC = {
-    "fwd_bf16": {"bytes": 201416576 + 45444864,
-                "src_sha256": "9ba5d9b7326139ffba4fa3338bd3f4820dc74b5165666d34e1c67d6c5e69743b"},
-    "bwd_dkdv_bf16": {"bytes": 270739712 + 215204736,
-                     "src_sha256": "52cb748f4f5dbe0285a2f6e4646a375b09c973419bd1b8dc981c174d0c9db3a3"},
-    "bwd_dq_bf16": {"bytes": 336833024 + 108038016,
-                   "src_sha256": "f60af3f7f29555b610dd3f2170c3b0d832708633e4b39ef9e69d552cf3659351"},
+    "fwd_bf16": {"bytes": 201439104 + 45610624,
+                "src_sha256": "4fa05ef15dae16eef945402bf2d68bb070310270cf2644410f960675ae80837f"},
+    "bwd_dkdv_bf16": {"bytes": 270648832 + 215226752,
+                     "src_sha256": "56e1b2c5fc36f36544a7650bbb85c7adea8f0e3cb8e1966f72661a2b9741b0c1"},
+    "bwd_dq_bf16": {"bytes": 336801024 + 108525824,
+                   "src_sha256": "bd45c6dba97e1747f31ce388732ef8367b55e6e903d637375e298cc1be77c917"},
 }
 
 REFERENCE_BUDGET_S = 120.0  # wall-clock bound on the reference arm's timed steps

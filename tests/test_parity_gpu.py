@@ -315,35 +315,38 @@ def test_config_b8_h16_n2048_d128_causal_training_step(fa, dev):
         assert bool(torch.isfinite(got[t]).all()), t
 
 
-def test_backward_n4096_causal_sampled_heads(fa, dev):
-    """bf16 backward at N = 4096, causal (32 key tiles per head), B=1 H=20
-    d=128: whole sampled heads against the oracle, the backward handed the
-    oracle's stored O and LSE for those heads.  At this length the kernels
-    claim work in groups of 8 heads, and dQ walks the groups from the last
-    one back, so 20 heads (8 + 8 + 4) put a short group first in dQ and last
-    in dK/dV; the sampled heads lie in the short group and in a full one."""
+@pytest.mark.parametrize("causal,heads", [(True, (3, 18)), (False, (11,))])
+def test_backward_n4096_sampled_heads(fa, dev, causal, heads):
+    """bf16 backward at N = 4096 (32 key tiles per head), B=1 H=20 d=128:
+    whole sampled heads against the oracle, the backward handed the oracle's
+    stored O and LSE for those heads.  Under the causal mask the kernels
+    claim work in groups of 8 heads at this length, and dQ walks the groups
+    from the last one back, so 20 heads (8 + 8 + 4) put a short group first
+    in dQ and last in dK/dV; the sampled heads lie in the short group and in
+    a full one.  Without the mask every dQ tile sums 32 key tiles and every
+    dK/dV item 32 Q tiles."""
     import torch
     B, H, N, d = 1, 20, 4096, 128
     x = inputs(40, B, H, N, d)
     s = scale_for(d)
-    bw_heads = np.array([3, 18])
-    refs = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], True, s, heads=bw_heads,
+    bw_heads = np.array(heads)
+    refs = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], causal, s, heads=bw_heads,
                                 o_storage="bf16")[:3]
     q, k, v, do = (to_device_bf16(x[n + "_bits"], dev) for n in ("q", "k", "v", "do"))
-    o, lse = fa.attention_fwd(q, k, v, causal=True, scale=s)
+    o, lse = fa.attention_fwd(q, k, v, causal=causal, scale=s)
     sub = {n: x[n].reshape(B * H, 1, N, d)[bw_heads].reshape(1, len(bw_heads), N, d)
            for n in ("q", "k", "v")}
-    so, sl = oracle_o_lse_on_device(sub, True, s, dev)
+    so, sl = oracle_o_lse_on_device(sub, causal, s, dev)
     hi = torch.from_numpy(bw_heads).to(dev)
     o.view(B * H, N, d)[hi] = so.view(len(bw_heads), N, d)
     lse.view(B * H, N)[hi] = sl.view(len(bw_heads), N)
-    dq, dk, dv = fa.attention_bwd(q, k, v, o, do, lse, causal=True, scale=s)
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, do, lse, causal=causal, scale=s)
     torch.cuda.synchronize()
     got = {"dq": dq, "dk": dk, "dv": dv}
     for name, ref in zip(("dq", "dk", "dv"), refs):
         g = got[name].cpu().numpy().reshape(B * H, N, d)[bw_heads]
-        diagnostic(f"N = 4096 causal backward {name}", max_abs=max_abs(g, ref),
-                   rel_rms=rel_rms(g, ref))
+        diagnostic(f"N = 4096 {'causal' if causal else 'not causal'} backward {name}",
+                   max_abs=max_abs(g, ref), rel_rms=rel_rms(g, ref))
     _check_grads(got, refs, bw_heads, B, H, N, d)
     for t in (dq, dk, dv):
         assert bool(torch.isfinite(t).all())
